@@ -17,6 +17,12 @@ Prints one JSON line (rank 0).  Keys beyond the required ones:
               of every output inside the timed region
   rows        the other hot-path rows measured in the same run: permutes
               (GB/s), strided/dilated dgrad and wgrad layers, int8 fprop
+  l2_warm     the same step replayed without the L2 flush in between
+  check       seeded samples of every output the last timed step wrote,
+              compared with the CPU oracle (per-element bound)
+  device_status the library's device error word after every timed region
+              (a kernel whose bounded wait gave up would otherwise post a
+              faster time); any error ends the run with a non-zero exit code
 
 --impl reference times the CPU oracle on bounded samples of the same
 workload (there is no other implementation to run here).
@@ -45,15 +51,12 @@ from synthetic import (GROUPED_SWEEP, RESNET50_SWEEP, WORKLOADS, make_inputs,  #
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 512 << 20
 
-# DRAM traffic (read + write bytes) per launch of the implicit-GEMM kernel,
-# averaged over the fprop + dgrad launches of one step, from an ncu capture
-# of this benchmark's command.  Valid only for the kernel source it was
-# taken on (SHA-256 of conv_gemm.cu, first 16 hex digits); otherwise null.
 # DRAM bytes (read + written) per launch of the implicit-GEMM kernel: the mean
-# over the 10 fprop/dgrad launches of one bench step in an ncu launch-list
-# capture (dram__bytes_read.sum + dram__bytes_write.sum, cold caches; see
-# profiles/launches_resnet50_sweep_b128.md), keyed by the kernel source hash.
-# A changed kernel source reports null until it is measured again.
+# over the 10 fprop/dgrad launches of one step, each captured alone by ncu
+# (dram__bytes_read.sum + dram__bytes_write.sum, cold caches), keyed by the
+# kernel source hash (SHA-256 prefix of the kernel, its PTX wrappers and its
+# parameter header).  A changed kernel source reports null until it is
+# measured again.
 MEASURED_TRAFFIC = {"07bc1453b624b18c": 65.00e6}
 
 
@@ -333,6 +336,71 @@ def run_only(args):
                       "ms_per_call": a.elapsed_time(b) / max(1, args.steps)}), flush=True)
 
 
+def require_device_ok(igc, where):
+    """Reads (and clears) the library's device error word after a timed
+    region; a kernel that gave up a bounded wait records a code there and
+    exits early, which would otherwise show up as a faster time."""
+    torch.cuda.synchronize()
+    st = igc.igconv_get_device_status()
+    if st != 0:
+        print(f"bench: device status '{igc.igconv_status_string(st)}' after {where}",
+              file=sys.stderr, flush=True)
+        raise SystemExit(3)
+    return "ok"
+
+
+FRAC_BITS = {"f16": 10, "bf16": 7}
+MIN_NORMAL_EXP = {"f16": -14, "bf16": -126}
+
+
+def _elem_bound(ref, A, fmt):
+    """Per-element bound used by the parity tests: one unit in the last place
+    of the output format (fp32: 2^-23 relative) plus 2^-10 of sum |x*w|."""
+    import numpy as np
+    if fmt == "f32":
+        return np.abs(ref) * 2.0 ** -23 + 2.0 ** -10 * A
+    ax = np.abs(ref)
+    e = np.floor(np.log2(np.where(ax > 0, ax, 1.0)))
+    e = np.maximum(e, MIN_NORMAL_EXP[fmt])
+    return np.ldexp(1.0, (e - FRAC_BITS[fmt]).astype(np.int64)) + 2.0 ** -10 * A
+
+
+def check_outputs(layers, samples, seed):
+    """Compares `samples` seeded elements of each output of every layer (Y,
+    dX, dW as the last timed step left them) with the CPU oracle on the same
+    inputs.  Run outside every timed region."""
+    import numpy as np
+
+    import oracle
+    oracle.build()
+    worst, count, failed = 0.0, 0, []
+    for i, L in enumerate(layers):
+        X64 = L.cpu["X"].to(torch.float64).numpy()
+        W64 = L.cpu["W"].to(torch.float64).numpy()
+        dY64 = L.cpu["dY"].to(torch.float64).numpy()
+        b64 = L.cpu["bias"].to(torch.float64).numpy() if L.bias else None
+        for kind, out, fmt in (("fprop", L.Y, L.dtype), ("dgrad", L.dX, L.dtype),
+                               ("wgrad", L.dW, L.dw_dtype)):
+            flat = out.reshape(-1)
+            idx = sample_indices(flat.numel(), samples, seed + 31 * i).numpy()
+            got = flat[torch.from_numpy(idx).to(flat.device)].to(torch.float64).cpu().numpy()
+            if kind == "fprop":
+                ref, A = oracle.fprop(L.pb, X64, W64, bias=b64, relu=L.relu, idx=idx,
+                                      want_abs=True)
+            elif kind == "dgrad":
+                ref, A = oracle.dgrad(L.pb, dY64, W64, idx=idx, want_abs=True)
+            else:
+                ref, A = oracle.wgrad(L.pb, X64, dY64, idx=idx, want_abs=True)
+            ratio = float(np.max(np.abs(got - ref) / _elem_bound(ref, A, fmt)))
+            if not np.isfinite(got).all() or ratio > 1.0:
+                failed.append(f"{L.name}:{kind}")
+            worst = max(worst, ratio)
+            count += idx.size
+    return {"checked": not failed, "samples_per_pass": samples, "elements": count,
+            "max_err_over_bound": worst, "failed": failed,
+            "bound": "|err_i| <= ulp(out_i) + 2^-10 * sum|x*w|_i against the fp64 oracle"}
+
+
 def run_ours(args, rank, world, local_rank):
     import convolution_implicit_gemm_gb300 as igc
     device = torch.device("cuda", local_rank)
@@ -390,6 +458,28 @@ def run_ours(args, rank, world, local_rank):
             records.append([(kind, L, x.elapsed_time(y)) for kind, L, (x, y) in rec])
     torch.cuda.synchronize()
     clk = clocks.stop()
+    status = {"timed_steps": require_device_ok(igc, "the timed steps")}
+    check = None
+    if rank == 0 and not args.no_check:
+        check = check_outputs(layers, args.check_samples, 777)
+        if not check["checked"]:
+            print(f"bench: outputs differ from the oracle: {check}", file=sys.stderr, flush=True)
+            raise SystemExit(4)
+    # the same step with L2 left warm between replays (no flush)
+    warm_ms, warm_records = [], []
+    for _ in range(min(args.steps, 50)):
+        if graph is not None:
+            graph.g.replay()
+            torch.cuda.synchronize()
+            warm_ms.append(graph.step_ms())
+            warm_records.append(graph.call_ms())
+        else:
+            rec = []
+            a, b = timed_launches(lambda: step(rec), stream)
+            torch.cuda.synchronize()
+            warm_ms.append(a.elapsed_time(b))
+            warm_records.append([(kind, L, x.elapsed_time(y)) for kind, L, (x, y) in rec])
+    status["l2_warm_steps"] = require_device_ok(igc, "the L2-warm steps")
     if world > 1:
         torch.distributed.barrier()
     total_ms = sum(step_ms)
@@ -425,6 +515,7 @@ def run_ours(args, rank, world, local_rank):
             torch.cuda.synchronize()
             e2e_ms += a.elapsed_time(b)
         e2e_ms /= max(1, args.e2e_steps)
+        status["e2e"] = require_device_ok(igc, "the end-to-end steps")
         e2e = {"value": step_flops / (e2e_ms * 1e-3) / 1e12 * world, "unit": "TFLOP/s",
                "h2d_bytes_per_step": sum(L.h2d for L in layers),
                "d2h_bytes_per_step": sum(L.d2h for L in layers),
@@ -433,6 +524,7 @@ def run_ours(args, rank, world, local_rank):
     rows = None
     if not args.no_rows and rank == 0:
         rows = measure_rows(args, device, stream)
+        status["rows"] = require_device_ok(igc, "the rows")
 
     # reduce across ranks: max time, summed work
     t = torch.tensor([total_ms], dtype=torch.float64, device=device)
@@ -444,9 +536,24 @@ def run_ours(args, rank, world, local_rank):
     layer_rows = {n: {k: {"us": v * 1e3,
                           "TFLOP/s": next(L.flops for L in layers if L.name == n) / (v * 1e-3) / 1e12}
                       for k, v in d.items()} for n, d in per_layer.items()}
+    warm_layers = {}
+    for rec in warm_records:
+        for kind, L, ms in rec:
+            warm_layers.setdefault(L.name, {}).setdefault(kind, 0.0)
+            warm_layers[L.name][kind] += ms / len(warm_records)
+    l2_warm = None
+    if warm_ms:
+        wm = sum(warm_ms) / len(warm_ms)
+        l2_warm = {"value": step_flops * world / (wm * 1e-3) / 1e12, "ms_per_step": wm,
+                   "steps": len(warm_ms),
+                   "layers": {n: {k: {"us": v * 1e3,
+                                      "TFLOP/s": next(L.flops for L in layers if L.name == n)
+                                      / (v * 1e-3) / 1e12}
+                                  for k, v in d.items()} for n, d in warm_layers.items()}}
     launch = ("CUDA graph of the step's 15 calls (20 kernels), replayed once per step"
               if graph is not None else "stream launches")
     return dict(layers=layers, value=value, ms_per_step=ms_per_step, clocks=clk, e2e=e2e,
+                status=status, check=check, l2_warm=l2_warm,
                 launch=launch,
                 layer_rows=layer_rows,
                 pass_tflops={k: pass_flops[k] / (pass_ms[k] * 1e-3) / 1e12 for k in pass_ms},
@@ -725,7 +832,8 @@ def workload_config(args):
                         % (args.batch or 128),
             "global_batch": (args.batch or 128),
             "passes": ["fprop", "dgrad", "wgrad"], "layers": 5,
-            "l2": "flushed between timed steps (512 MiB write)",
+            "l2": "flushed between timed steps (512 MiB write); the same step with L2 left "
+                  "warm is reported under l2_warm",
             "parallelism": "replicas" if args.gpus > 1 else "single GPU"}
 
 
@@ -743,6 +851,9 @@ def main():
     ap.add_argument("--no-graph", action="store_true",
                     help="time the step's calls as plain stream launches instead of a CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-check", action="store_true",
+                    help="skip the sampled oracle check of the last timed step's outputs")
+    ap.add_argument("--check-samples", type=int, default=200)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-step-s", type=float, default=3.0)
     ap.add_argument("--only", default=None, metavar="LAYER:PASS",
@@ -772,13 +883,27 @@ def main():
     peaks, peak_src = load_peaks()
     gemm_flops, gemm_ms, gemm_launches = res["gemm"]
     achieved = gemm_flops / (gemm_ms * 1e-3) / 1e12
-    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    # The peak of the regime the step ran in: the burst figure (cuBLAS timed
+    # briefly at the maximum clock) when the sampled SM clock stayed at the
+    # maximum during the timed steps, else the sustained one (a seconds-long
+    # cuBLAS loop under the power cap, at a lower clock).
+    burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    sm_mhz = res["clocks"].get("sm_mhz")
+    sm_max = res["clocks"].get("sm_max_mhz") or peaks.get("sm_max_mhz")
+    at_max = sm_mhz is not None and bool(sm_max) and sm_mhz >= 0.97 * float(sm_max)
+    peak = burst if at_max else sustained
     src_hash = kernel_source_hash()
     traffic = MEASURED_TRAFFIC.get(src_hash)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic,
                 "kernel": "conv_gemm_kernel (fprop + dgrad launches of the step)",
-                "peak_source": f"{peak_src} sustained bf16 (cuBLAS loop under the power cap)",
+                "peak_kind": "burst" if at_max else "sustained",
+                "peak_source": (f"{peak_src} bf16 {'burst (cuBLAS at the maximum clock)' if at_max else 'sustained (cuBLAS loop under the power cap)'}"
+                                f"; chosen because the median SM clock during the timed steps "
+                                f"was {sm_mhz} MHz against a maximum of {sm_max} MHz"),
+                "peak_burst": burst, "frac_burst": achieved / burst,
+                "peak_sustained": sustained, "frac_sustained": achieved / sustained,
                 "launches_per_step": gemm_launches // max(1, args.steps),
                 "kernel_source": src_hash}
     line = {"metric": METRIC, "value": res["value"], "unit": "TFLOP/s", "n_gpus": world,
@@ -790,7 +915,8 @@ def main():
             "passes": res["pass_tflops"], "layers": res["layer_rows"], "roofline": roofline,
             "clocks": res["clocks"],
             "gpu_launches": res["launches"], "e2e": res["e2e"], "rows": res["rows"],
-            "launch": res["launch"]}
+            "l2_warm": res["l2_warm"], "check": res["check"],
+            "device_status": res["status"], "launch": res["launch"]}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args)
     if rank == 0:

@@ -15,6 +15,7 @@
 // different host threads) race on it and must be serialised by the caller.
 // Each call overwrites every partial it later reads, so the array never needs
 // clearing.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -25,25 +26,68 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_wgrad_scratch[IGCONV_WGRAD_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxScratchDevices = 64;
-std::mutex g_scratch_mu;
-void* g_scratch_ptr[kMaxScratchDevices] = {};
+typedef CUresult (*PFN_ctxGetCurrent)(CUcontext*);
+typedef CUresult (*PFN_ctxGetId)(CUcontext, unsigned long long*);
 
-// Device address of the scratch array on the current device.  In host code
-// the array's name only stands in for the symbol, so the address is looked
-// up once per device, with that device current, and cached.
+constexpr int kMaxScratchDevices = 64;
+struct ScratchSlot {
+  unsigned long long ctx_id;  // unique ID of the context the address belongs to
+  void* ptr;
+};
+std::mutex g_scratch_mu;
+ScratchSlot g_scratch[kMaxScratchDevices] = {};
+PFN_ctxGetCurrent g_ctx_current = nullptr;
+PFN_ctxGetId g_ctx_id = nullptr;
+
+// Unique ID of the calling thread's current context (0 when none is current
+// yet).  cudaDeviceReset destroys a device's primary context and the next
+// runtime call creates a new one with a new ID, in which the array has a new
+// address.
+bool current_context_id(unsigned long long* id) {
+  *id = 0;
+  CUcontext ctx = nullptr;
+  if (g_ctx_current(&ctx) != CUDA_SUCCESS) return false;
+  return ctx == nullptr || g_ctx_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of the scratch array in the current device's context.  In
+// host code the array's name only stands in for the symbol, so the address is
+// looked up with cudaGetSymbolAddress the first time a context of a device
+// calls, and cached with that context's ID; a call from a new context (after
+// cudaDeviceReset) looks it up again.
 igconv_status_t scratch_address(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxScratchDevices)
     return IGCONV_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
+  if (!g_ctx_current || !g_ctx_id) {
+    void* f1 = nullptr;
+    void* f2 = nullptr;
+    cudaDriverEntryPointQueryResult q1, q2;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault,
+                                         &q1) != cudaSuccess ||
+        q1 != cudaDriverEntryPointSuccess ||
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) !=
+            cudaSuccess ||
+        q2 != cudaDriverEntryPointSuccess)
+      return IGCONV_ERR_CUDA;
+    g_ctx_current = reinterpret_cast<PFN_ctxGetCurrent>(f1);
+    g_ctx_id = reinterpret_cast<PFN_ctxGetId>(f2);
+  }
+  unsigned long long id = 0;
+  if (!current_context_id(&id)) return IGCONV_ERR_CUDA;
+  ScratchSlot& slot = g_scratch[dev];
+  if (slot.ptr == nullptr || id == 0 || slot.ctx_id != id) {
+    // the lookup also makes the device's primary context current if no
+    // runtime call has done so yet
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_wgrad_scratch) != cudaSuccess || p == nullptr)
       return IGCONV_ERR_CUDA;
-    g_scratch_ptr[dev] = p;
+    if (!current_context_id(&id) || id == 0) return IGCONV_ERR_CUDA;
+    slot.ctx_id = id;
+    slot.ptr = p;
   }
-  *out = g_scratch_ptr[dev];
+  *out = slot.ptr;
   return IGCONV_OK;
 }
 

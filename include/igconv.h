@@ -206,9 +206,11 @@ IGCONV_API igconv_status_t conv2d_wgrad(const igconv_problem_t *prob, igconv_dty
  * loading the library holds until exit.  It allocates nothing and frees
  * nothing.
  *   Arguments: as conv2d_wgrad, without workspace / workspace_bytes.
- *   The first call on a device looks up the array's device address (with
- *   that device current) and caches it; make that first call before any
- *   stream capture on the device.
+ *   The first call in a device's context looks up the array's device
+ *   address (with that device current) and caches it with the context's ID;
+ *   a call from a new context (after cudaDeviceReset) looks it up again.
+ *   Make the first call on a device, and the first after a reset, before
+ *   any stream capture on that device.
  *   All calls on a device share the array: calls whose kernels can overlap
  *   on the GPU (other streams, other host threads) race and must be
  *   serialised by the caller.  Every partial a call reads was written by the

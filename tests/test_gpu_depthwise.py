@@ -9,8 +9,10 @@ variant (3x3, 5x5 at strides 1 and 2, 7x7 at stride 1), the generic kernel
 (rectangular filters, dilation, stride 3), the strided-dgrad phase kernel
 with its tap tables (strides dividing 8) and without them (stride 3), its
 shared-word row loop (2 or 3 column taps per phase on consecutive dY
-columns: 3x3, 5x5 and 7x7 at stride 2) and the per-tap loop beside it (one
-or four taps, column dilation 2),
+columns: 3x3, 5x5 and 7x7 at stride 2, and 3x3 at stride 2 with dilation 2,
+whose taps of a phase are also consecutive) and the per-tap loop beside it
+(one tap per phase, four taps at stride 4 x 2, and two non-consecutive taps
+per phase at stride 2 with column dilation 3),
 channel counts below and between the 32-channel chunks, images whose row
 count is not a multiple of the 8-row blocks, and ragged column tiles."""
 import numpy as np
@@ -44,6 +46,7 @@ SHAPES = [
     dw(1, 9, 11, 64, 7, 7, (3, 3), (2, 2)),             # 7x7 s2: generic
     dw(2, 18, 21, 48, 3, 3, (1, 1), (1, 2)),            # stride 1 x 2: dgrad phases in w only
     dw(1, 21, 17, 16, 3, 3, (2, 2), (2, 2), (2, 2)),    # stride 2 + dilation 2
+    dw(1, 17, 19, 24, 3, 3, (3, 3), (2, 2), (3, 3)),    # stride 2 + dilation 3: taps 2 apart
     dw(2, 11, 30, 24, 4, 2, (1, 0), (4, 2)),            # stride 4 x 2, even filter
     dw(3, 1, 1, 16, 1, 1),                              # 1x1 pixel images
     dw(1, 5, 5, 8, 5, 5),                               # P = Q = 1

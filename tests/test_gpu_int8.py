@@ -69,3 +69,37 @@ def test_int8_worst_case_accumulation_is_exact(C, num_terms):
     bias = torch.from_numpy((-acc + j).astype(np.int32))
     got = run_int8(pb, X, Wt, bias, 1.0, 1.0, 1.0, False)
     np.testing.assert_array_equal(got.reshape(2, K), np.stack([j, j]).astype(np.int8))
+
+
+@pytest.mark.parametrize("C", [128, 448])
+@pytest.mark.parametrize("pattern", ["same_sign", "rise_then_cancel"])
+def test_int8_odd_products_near_2_24_are_exact(C, pattern):
+    """Products 127 * +-127 = +-16129 are odd, so every partial sum over an odd
+    number of them is odd: an adder that dropped the lowest significand bit of
+    a sum between 2^23 and 2^24 would show.  An accumulator collects at most
+    1024 products (16 blocks of 64 channels), 1024 * 16129 = 16,516,096 <
+    2^24, which needs all 24 bits of the fp32 significand.  'same_sign' drives
+    every accumulator to its largest sum; 'rise_then_cancel' adds the first
+    five taps with one sign and the last four with the other, so the partial
+    sums climb and the exact total is small.  With M = 1 and bias = -acc + j
+    the output is j only if the accumulator is exact to the unit."""
+    K = 16
+    pb = problem(2, 3, 3, C, K, 3, 3)          # P = Q = 1: every output sees every tap
+    X = torch.full((2, 3, 3, C), 127, dtype=torch.int8)
+    sgn_k = np.array([1 if k % 2 == 0 else -1 for k in range(K)], dtype=np.int64)
+    if pattern == "same_sign":
+        tap_sign = np.ones(9, dtype=np.int64)
+    else:
+        tap_sign = np.array([1] * 5 + [-1] * 4, dtype=np.int64)
+    Wn = (127 * sgn_k[:, None, None] * tap_sign[None, :, None]
+          * np.ones((K, 9, C), dtype=np.int64)).reshape(K, 3, 3, C)
+    Wt = torch.from_numpy(Wn.astype(np.int8))
+    acc = 127 * Wn.reshape(K, -1).sum(axis=1)
+    assert np.all(acc % 2 == 0) and np.abs(acc).max() < 2 ** 31
+    j = np.arange(K, dtype=np.int64) - 8
+    bias = torch.from_numpy((-acc + j).astype(np.int32))
+    got = run_int8(pb, X, Wt, bias, 1.0, 1.0, 1.0, False)
+    np.testing.assert_array_equal(got.reshape(2, K), np.stack([j, j]).astype(np.int8))
+    # the oracle agrees on the same inputs (its accumulation is int64)
+    ref = oracle.fprop_int8(pb, X.numpy(), Wt.numpy(), bias.numpy(), 1.0, 1.0, 1.0, relu=False)
+    np.testing.assert_array_equal(got, ref)

@@ -10,6 +10,7 @@ import pytest
 
 import oracle as oracle_mod
 from tests import test_oracle_3d_pins as pins3d
+from tests import test_oracle_abs_pins as apins
 from tests import test_oracle_grouped_pins as gpins
 from tests import test_oracle_pins as pins
 
@@ -71,6 +72,42 @@ MUTANTS = [
      "int64_t di = (((int64_t)n * W + w) * H + h) * C + c;\n                    memcpy", 0),
 ]
 
+# Slips in the second output, A = |alpha| * sum |x*w| (the tolerance scale).
+# Each entry is (name, [(text to find, replacement, occurrence), ...]); the
+# edits are applied in order.  Occurrence i of the A store is pass i in source
+# order: fprop, dgrad, wgrad, grouped fprop / dgrad / wgrad, 3D fprop / dgrad /
+# wgrad.
+A_STORE = "if (t->A) t->A[j] = fabs(t->alpha) * asum;"
+_PASSES = ["fprop", "dgrad", "wgrad", "grouped fprop", "grouped dgrad", "grouped wgrad",
+           "3d fprop", "3d dgrad", "3d wgrad"]
+ABS_MUTANTS = [
+    (f"{name} A of the signed sum", [(A_STORE, "if (t->A) t->A[j] = fabs(t->alpha * sum);", i)])
+    for i, name in enumerate(_PASSES)
+] + [
+    (f"{name} A without |alpha|", [(A_STORE, "if (t->A) t->A[j] = asum;", i)])
+    for i, name in enumerate(_PASSES)
+] + [
+    ("fprop A as a sum of magnitudes", [("asum += fabs(x * f);", "asum += fabs(x) + fabs(f);", 0)]),
+    ("fprop A as a product of sums", [
+        ("double sum = 0.0, asum = 0.0;", "double sum = 0.0, asum = 0.0, sx = 0.0, sf = 0.0;", 0),
+        ("asum += fabs(x * f);", "sx += fabs(x); sf += fabs(f);", 0),
+        (A_STORE, "asum = sx * sf; " + A_STORE, 0)]),
+    ("dgrad A from the wrong input channel", [
+        ("asum += fabs(g * f);",
+         "asum += fabs(g * t->Wt[(((int64_t)k * p->R + r) * p->S + s) * p->C + (c + 1) % p->C]);",
+         0)]),
+    ("wgrad A from the previous image", [
+        ("asum += fabs(g * x);",
+         "asum += fabs(g * t->X[(((int64_t)((n + 1) % p->N) * p->H + h) * p->W + w) * p->C + c]);",
+         0)]),
+    ("grouped dgrad A over every output channel", [
+        ("asum += fabs(gy * f);",
+         "for (int k2 = 0; k2 < p->K; ++k2) asum += fabs(t->A_in[(((int64_t)n * t->P + pp) * t->Q"
+         " + q) * p->K + k2] * f) / t->Kg;", 0)]),
+    ("A includes the bias", [(A_STORE, "if (t->A) t->A[j] = fabs(t->alpha) * asum + "
+                              "(t->bias ? fabs(t->bias[k]) : 0.0);", 0)]),
+]
+
 PIN_CALLS = [
     (pins.test_output_size_golden, {}),
     (pins.test_output_size_counts_valid_windows, {}),
@@ -96,7 +133,15 @@ PIN_CALLS = [
   + [(pins3d.test_separable_filter_is_sum_of_2d, {"pb": pb}) for pb in pins3d.PROBLEMS_3D] \
   + [(pins3d.test_3d_adjoint_identities_exact, {"pb": pb}) for pb in pins3d.PROBLEMS_3D] \
   + [(gpins.test_grouped_is_dense_with_block_diagonal_filter, {"pb": pb, "groups": g})
-     for pb, g in gpins.GROUPED_PROBLEMS]
+     for pb, g in gpins.GROUPED_PROBLEMS] \
+  + [(fn, {"pb": pb}) for pb in apins.PROBLEMS_2D
+     for fn in (apins.test_fprop_abs_sum_is_im2col_of_magnitudes,
+                apins.test_dgrad_abs_sum_is_col2im_of_magnitudes,
+                apins.test_wgrad_abs_sum_is_im2col_of_magnitudes)] \
+  + [(apins.test_grouped_abs_sums_are_torch_convs_of_magnitudes, {"pb": pb, "groups": g})
+     for pb, g in gpins.GROUPED_PROBLEMS] \
+  + [(apins.test_3d_abs_sums_are_torch_convs_of_magnitudes, {"pb": pb})
+     for pb in pins3d.PROBLEMS_3D]
 
 
 def _first_failing_pin():
@@ -112,15 +157,19 @@ def test_mutant_catalogue_applies_to_current_source():
     src = open(SRC).read()
     for name, find, _, occ in MUTANTS:
         assert src.count(find) > occ, f"mutant '{name}' no longer matches the source"
+    for name, edits in ABS_MUTANTS:
+        for find, _, occ in edits:
+            assert src.count(find) > occ, f"mutant '{name}' no longer matches the source"
 
 
-@pytest.mark.parametrize("name,find,repl,occ", MUTANTS, ids=[m[0] for m in MUTANTS])
-def test_pins_reject_mutant(tmp_path, name, find, repl, occ):
-    src = open(SRC).read()
+def _apply(src, find, repl, occ):
     pos = -1
     for _ in range(occ + 1):
         pos = src.index(find, pos + 1)
-    mutated = src[:pos] + repl + src[pos + len(find):]
+    return src[:pos] + repl + src[pos + len(find):]
+
+
+def _assert_rejected(tmp_path, name, mutated):
     c_path = tmp_path / "mutant.c"
     so_path = tmp_path / "libmutant.so"
     c_path.write_text(mutated)
@@ -129,3 +178,16 @@ def test_pins_reject_mutant(tmp_path, name, find, repl, occ):
     with oracle_mod.use_library(str(so_path)):
         caught = _first_failing_pin()
     assert caught is not None, f"no pin rejects the mutant '{name}'"
+
+
+@pytest.mark.parametrize("name,find,repl,occ", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_reject_mutant(tmp_path, name, find, repl, occ):
+    _assert_rejected(tmp_path, name, _apply(open(SRC).read(), find, repl, occ))
+
+
+@pytest.mark.parametrize("name,edits", ABS_MUTANTS, ids=[m[0] for m in ABS_MUTANTS])
+def test_pins_reject_abs_sum_mutant(tmp_path, name, edits):
+    src = open(SRC).read()
+    for find, repl, occ in edits:
+        src = _apply(src, find, repl, occ)
+    _assert_rejected(tmp_path, name, src)

@@ -6,9 +6,11 @@ a caller workspace.
 
 This file is collected last on purpose, so that a run stopping at its first
 failure has already run every other test.  It calls the entry point through
-the C ABI and checks it against conv2d_wgrad (the workspace entry point) on
-two calls in a row with different problems, so a stale array from the first
-call cannot make the second pass."""
+the C ABI on two calls in a row with different problems, so a stale array
+from the first call cannot make the second pass, and checks each result
+bit for bit against conv2d_wgrad (the workspace entry point), exactly
+against the oracle on integer data, and within the tolerance on random
+data."""
 import ctypes
 
 import pytest
@@ -17,7 +19,7 @@ import torch
 import convolution_implicit_gemm_gb300 as igc
 import oracle
 from synthetic import WORKLOADS
-from tests.helpers import assert_close, device_ok, f64, inputs, problem, to_f64
+from tests.helpers import assert_close, assert_exact, device_ok, f64, inputs, problem, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -63,10 +65,17 @@ def test_noalloc_matches_workspace_entry_point_on_consecutive_calls():
         rc = _call_noalloc(pb, dt, dwt, X, dY, Cin, dW, alpha, beta)
         assert rc == 0, igc.igconv_status_string(rc)
         device_ok()
-        _, A = oracle.wgrad(pb, f64(inp["X"]), f64(inp["dY"]),
-                            Cin=f64(inp["C_wgrad"]) if beta != 0.0 else None, alpha=alpha,
-                            beta=beta, want_abs=True)
-        assert_close(to_f64(dW), to_f64(ref), A, dwt, f"no-alloc wgrad {pb['N']}x{pb['H']}")
+        want, A = oracle.wgrad(pb, f64(inp["X"]), f64(inp["dY"]),
+                               Cin=f64(inp["C_wgrad"]) if beta != 0.0 else None, alpha=alpha,
+                               beta=beta, want_abs=True)
+        what = f"no-alloc wgrad {pb['N']}x{pb['H']}"
+        # the same plan and kernels as the workspace entry point: the same bits
+        assert torch.equal(dW.view(torch.uint8), ref.view(torch.uint8)), \
+            f"{what}: differs from conv2d_wgrad"
+        if recipe == "int_uniform":
+            # integer data whose sums stay below 2^24: exact against the oracle
+            assert_exact(to_f64(dW), want, dwt, what)
+        assert_close(to_f64(dW), want, A, dwt, what)
 
 
 def test_noalloc_rejects_problems_beyond_the_scratch():
