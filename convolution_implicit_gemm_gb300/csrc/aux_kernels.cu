@@ -22,8 +22,10 @@ cudaError_t status_word_address(unsigned int** ptr) {
 // ---------------------------------------------------------------------------
 // Batched transpose: dst[b][j][i] = src[b][i][j], i < rows, j < cols.
 //   nchw_to_nhwc: rows = C, cols = H*W;  nhwc_to_nchw: rows = H*W, cols = C.
-// 64 x 64 element tiles staged in shared memory; 16-byte vector loads along
-// j and 16-byte vector stores along i whenever row pitches allow.
+// General form (any element size, extent or alignment): 64 x 64 element
+// tiles staged in shared memory; 16-byte vector loads along j and 16-byte
+// vector stores along i whenever row pitches allow.  The common case takes
+// the register transpose further down.
 // ---------------------------------------------------------------------------
 template <typename T>
 __global__ void __launch_bounds__(256) transpose_kernel(const T* __restrict__ src,
@@ -83,8 +85,101 @@ __global__ void __launch_bounds__(256) transpose_kernel(const T* __restrict__ sr
   }
 }
 
+// ---------------------------------------------------------------------------
+// Register transpose for 2- and 4-byte elements when rows and cols are
+// multiples of the vector width V = 16 / sizeof(T) and both tensors are
+// 16-byte aligned.  Each thread moves one V x V block: V 16-byte loads (rows
+// i .. i+V-1, columns j .. j+V-1), a transpose in registers, V 16-byte
+// stores (rows j .. j+V-1 of dst, columns i .. i+V-1).  No shared memory and
+// no barrier, so a thread keeps all V loads in flight at once.  The lanes of
+// a warp form a 4 x 8 grid of blocks (4 along i, 8 along j): every load
+// instruction reads four runs of 8 * 16 = 128 contiguous bytes, every store
+// instruction writes eight runs of 4 * 16 = 64 bytes (two whole sectors).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void transpose_block(uint4 (&r)[8], uint4 (&o)[8]) {
+  // 8 x 8 block of 16-bit elements: r[k] holds row k, o[m] receives column m.
+  // Step 1 swaps 16-bit halves between rows 2q and 2q+1, so that word p of
+  // t[2q + e] holds rows (2q, 2q+1) of column 2p + e.  Step 2 is then a 4 x 4
+  // transpose of 32-bit words for each e (register renaming only).
+  uint32_t t[8][4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t a[4] = {r[2 * q].x, r[2 * q].y, r[2 * q].z, r[2 * q].w};
+    const uint32_t b[4] = {r[2 * q + 1].x, r[2 * q + 1].y, r[2 * q + 1].z, r[2 * q + 1].w};
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      t[2 * q][p] = __byte_perm(a[p], b[p], 0x5410);      // low halves: column 2p
+      t[2 * q + 1][p] = __byte_perm(a[p], b[p], 0x7632);  // high halves: column 2p + 1
+    }
+  }
+#pragma unroll
+  for (int p = 0; p < 4; ++p)
+#pragma unroll
+    for (int e = 0; e < 2; ++e)
+      o[2 * p + e] = make_uint4(t[e][p], t[2 + e][p], t[4 + e][p], t[6 + e][p]);
+}
+
+__device__ __forceinline__ void transpose_block(uint4 (&r)[4], uint4 (&o)[4]) {
+  // 4 x 4 block of 32-bit elements: word m of row k is element (k, m)
+  o[0] = make_uint4(r[0].x, r[1].x, r[2].x, r[3].x);
+  o[1] = make_uint4(r[0].y, r[1].y, r[2].y, r[3].y);
+  o[2] = make_uint4(r[0].z, r[1].z, r[2].z, r[3].z);
+  o[3] = make_uint4(r[0].w, r[1].w, r[2].w, r[3].w);
+}
+
+template <int V>
+__global__ void __launch_bounds__(256) transpose_reg_kernel(const uint8_t* __restrict__ src,
+                                                            uint8_t* __restrict__ dst,
+                                                            long long batch, long long rows,
+                                                            long long cols, long long tiles_i,
+                                                            long long tiles_j) {
+  constexpr int EB = 16 / V;  // element bytes
+  constexpr int A = 4, B = 8;  // blocks per warp tile along i and j
+  const long long warp_tile = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const long long per_batch = tiles_i * tiles_j;
+  if (warp_tile >= batch * per_batch) return;
+  const int lane = threadIdx.x & 31;
+  const long long bidx = warp_tile / per_batch;
+  const long long t = warp_tile - bidx * per_batch;
+  const long long ti = t / tiles_j;
+  const long long tj = t - ti * tiles_j;
+  const long long i = (ti * A + (lane / B)) * V;
+  const long long j = (tj * B + (lane % B)) * V;
+  if (i >= rows || j >= cols) return;
+  const uint8_t* s = src + (bidx * rows * cols + i * cols + j) * EB;
+  uint8_t* d = dst + (bidx * rows * cols + j * rows + i) * EB;
+  uint4 r[V], o[V];
+#pragma unroll
+  for (int k = 0; k < V; ++k)
+    r[k] = __ldcs(reinterpret_cast<const uint4*>(s + static_cast<long long>(k) * cols * EB));
+  transpose_block(r, o);
+#pragma unroll
+  for (int m = 0; m < V; ++m)
+    __stcs(reinterpret_cast<uint4*>(d + static_cast<long long>(m) * rows * EB), o[m]);
+}
+
 cudaError_t launch_batched_transpose(const void* src, void* dst, long long batch, long long rows,
                                      long long cols, int elem_bytes, cudaStream_t s) {
+  const uintptr_t sa0 = reinterpret_cast<uintptr_t>(src), da0 = reinterpret_cast<uintptr_t>(dst);
+  if ((elem_bytes == 2 || elem_bytes == 4) && ((sa0 | da0) & 15) == 0) {
+    const int V = 16 / elem_bytes;
+    if (rows % V == 0 && cols % V == 0) {
+      const long long tiles_i = (rows + 4 * V - 1) / (4 * V);
+      const long long tiles_j = (cols + 8 * V - 1) / (8 * V);
+      const long long warps = batch * tiles_i * tiles_j;
+      const long long blocks = (warps + 7) / 8;
+      if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+      if (V == 8)
+        transpose_reg_kernel<8><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+            static_cast<const uint8_t*>(src), static_cast<uint8_t*>(dst), batch, rows, cols,
+            tiles_i, tiles_j);
+      else
+        transpose_reg_kernel<4><<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+            static_cast<const uint8_t*>(src), static_cast<uint8_t*>(dst), batch, rows, cols,
+            tiles_i, tiles_j);
+      return cudaGetLastError();
+    }
+  }
   const dim3 grid(static_cast<unsigned>((cols + 63) / 64), static_cast<unsigned>((rows + 63) / 64),
                   static_cast<unsigned>(batch));
   const uintptr_t sa = reinterpret_cast<uintptr_t>(src), da = reinterpret_cast<uintptr_t>(dst);

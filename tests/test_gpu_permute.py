@@ -1,5 +1,10 @@
 """GPU parity of the NCHW <-> NHWC permute kernels against the oracle's
-permutes: bit-exact, for every element size, aligned and ragged shapes."""
+permutes: bit-exact, for every element size, aligned and ragged shapes.
+
+2- and 4-byte elements whose two transposed extents are multiples of 8 (or
+4) take the register-transpose kernel; (3, 24, 5, 8), (2, 40, 4, 6) and
+(2, 12, 3, 4) give it warp tiles cut short in both directions.  Other shapes,
+other element sizes and unaligned pointers take the shared-memory kernel."""
 import numpy as np
 import pytest
 import torch
@@ -11,7 +16,7 @@ from tests.helpers import device_ok, guarded_empty
 pytestmark = pytest.mark.gpu
 
 SHAPES = [(2, 64, 8, 8), (3, 3, 7, 7), (1, 130, 5, 13), (4, 64, 56, 56), (1, 1, 1, 1),
-          (2, 17, 64, 3)]
+          (2, 17, 64, 3), (3, 24, 5, 8), (2, 40, 4, 6), (2, 12, 3, 4), (1, 256, 14, 14)]
 DTYPES = [torch.int8, torch.float16, torch.float32, torch.float64]
 
 
