@@ -587,12 +587,21 @@ def measure_rows(args, device, stream):
     src = torch.randn((N, C, H, W), device=device).to(torch.bfloat16)
     dst = torch.empty((N, H, W, C), dtype=torch.bfloat16, device=device)
     nbytes = 2 * src.numel() * src.element_size()
-    ms = time_call(lambda: igc.nchw_to_nhwc(src, dst, N, C, H, W), stream, flush=flush)
-    rows["nchw_to_nhwc"] = {"GB/s": nbytes / (ms * 1e-3) / 1e9, "ms": ms,
-                            "shape": [N, C, H, W], "dtype": "bf16"}
-    ms = time_call(lambda: igc.nhwc_to_nchw(dst, src, N, C, H, W), stream, flush=flush)
-    rows["nhwc_to_nchw"] = {"GB/s": nbytes / (ms * 1e-3) / 1e9, "ms": ms,
-                            "shape": [N, C, H, W], "dtype": "bf16"}
+    peaks, peak_src = load_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    # a plain device copy of the same bytes: what one launch of this size can
+    # move (launch, ramp-up and tail weigh on a ~20 us kernel; the HBM peak
+    # was measured on a 2 GB copy)
+    copy_ms = time_call(lambda: dst.view(-1).copy_(src.view(-1)), stream, flush=flush)
+    copy_gbs = nbytes / (copy_ms * 1e-3) / 1e9
+    for name, fn in (("nchw_to_nhwc", lambda: igc.nchw_to_nhwc(src, dst, N, C, H, W)),
+                     ("nhwc_to_nchw", lambda: igc.nhwc_to_nchw(dst, src, N, C, H, W))):
+        ms = time_call(fn, stream, flush=flush)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        rows[name] = {"GB/s": gbs, "ms": ms, "shape": [N, C, H, W], "dtype": "bf16",
+                      "bytes": nbytes, "frac_hbm": gbs / hbm, "hbm_gbs": hbm,
+                      "hbm_source": peak_src, "copy_same_bytes_GB/s": copy_gbs,
+                      "frac_copy_same_bytes": gbs / copy_gbs}
     del src, dst
     # dgrad/wgrad-heavy layers (dilated and strided), all three passes
     for name in ("dilated_112x112_64to64_3x3_d2", "strided_112x112_64to64_3x3_s2",

