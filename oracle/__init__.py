@@ -30,6 +30,13 @@ Parity status of each function (what pins it, in ``tests/test_oracle_pins.py``):
                   depth 1 against the 2D passes, torch float64 autograd
   fprop_int8      pinned: closed-form requantisation cases (ties, saturation,
                   ReLU), exact accumulation against an int64 numpy einsum
+  dgrad_int8 /    pinned: equal to the pinned fp64 dgrad / wgrad on the same
+  wgrad_int8      integers, exact int64 adjoint identities with fprop_int8's
+                  accumulator, hand-computed wrap past 2^31, int64 numpy
+                  im2col products
+  abs sums (A)    pinned: equal to the passes run on |operands| by im2col /
+                  col2im products and torch convolutions (any route but the
+                  oracle's loops)
   f16/bf16 round  pinned: numpy float16 conversion, hand-constructed ties
   permutes        pinned: index formula, round trip
 """
@@ -105,6 +112,9 @@ def _bind(lib):
     lib.oracle_fprop_int8.argtypes = [ctypes.POINTER(_Problem), _P, _P, _P, _D, _D, _D,
                                       _I, _P, _I64, _P, _P, _I]
     lib.oracle_fprop_int8.restype = _I
+    lib.oracle_backward_int8.argtypes = [_I, ctypes.POINTER(_Problem), _P, _P, _P, _I64, _P,
+                                         _P, _I]
+    lib.oracle_backward_int8.restype = _I
     lib.oracle_requant_multiplier.argtypes = [_D, _D, _D]
     lib.oracle_requant_multiplier.restype = ctypes.c_float
     lib.oracle_requant.argtypes = [_I64, ctypes.c_float, _I]
@@ -384,6 +394,37 @@ def fprop_int8(pb: dict, X, Wt, bias, act_scale, w_scale, out_scale, relu=True,
         Y = Y.reshape(pb["N"], P, Q, pb["K"])
         acc = None if acc is None else acc.reshape(Y.shape)
     return (Y, acc) if want_acc else Y
+
+
+def _backward_int8(which, pb, a, b, idx, nthreads, want_acc, shape):
+    a = np.ascontiguousarray(a, dtype=np.int8)
+    b = np.ascontiguousarray(b, dtype=np.int8)
+    idx, count = _indices(idx, int(np.prod(shape)))
+    out = np.empty(count, np.int32)
+    acc = np.empty(count, np.int64) if want_acc else None
+    rc = _load().oracle_backward_int8(which, ctypes.byref(_problem(pb)), _ptr(a), _ptr(b),
+                                      _ptr(idx), count, _ptr(out), _ptr(acc),
+                                      nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("empty output size")
+    if idx is None:
+        out = out.reshape(shape)
+        acc = None if acc is None else acc.reshape(shape)
+    return (out, acc) if want_acc else out
+
+
+def dgrad_int8(pb: dict, dY, Wt, idx=None, nthreads=None, want_acc=False):
+    """int8 dgrad: dX [N][H][W][C] int32 (the exact sum modulo 2^32); with
+    want_acc also the exact int64 sums."""
+    return _backward_int8(1, pb, dY, Wt, idx, nthreads, want_acc,
+                          (pb["N"], pb["H"], pb["W"], pb["C"]))
+
+
+def wgrad_int8(pb: dict, X, dY, idx=None, nthreads=None, want_acc=False):
+    """int8 wgrad: dW [K][R][S][C] int32 (the exact sum modulo 2^32); with
+    want_acc also the exact int64 sums."""
+    return _backward_int8(2, pb, X, dY, idx, nthreads, want_acc,
+                          (pb["K"], pb["R"], pb["S"], pb["C"]))
 
 
 def requant_multiplier(act_scale: float, w_scale: float, out_scale: float) -> float:

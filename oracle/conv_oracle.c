@@ -1,6 +1,7 @@
 /*
  * conv_oracle.c -- the CPU oracle for 2D convolution (fprop, dgrad, wgrad,
- * dense and grouped, 3D, int8 fprop with requantisation) and the
+ * dense and grouped, 3D, int8 fprop with requantisation, int8 dgrad and
+ * wgrad with int32 results) and the
  * NCHW<->NHWC permutes.
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the library calls this code; only the
@@ -778,6 +779,114 @@ int oracle_fprop_int8(const oracle_problem *pb, const int8_t *X, const int8_t *W
     t.relu = relu;
     t.idx = idx; t.Y = Y; t.acc = acc;
     oracle_parallel(int8_elem, &t, count, nthreads);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* int8 data and weight gradients (int32 results)                            */
+/*   dX[n,h,w,c] = sum over (k, r, s) and the output position (p, q) that    */
+/*                 reads (h, w) through tap (r, s) of dY[n,p,q,k]*W[k,r,s,c] */
+/*   dW[k,r,s,c] = sum_{n,p,q} dY[n,p,q,k] * X[n, p*sh - ph + r*dh,          */
+/*                 q*sw - pw + s*dw, c]                                      */
+/* int8 operands, the sums taken exactly in int64 and delivered as int32:    */
+/* the value modulo 2^32 in two's complement, which is what an int32         */
+/* accumulator holds.  Sources: PyTorch quantized cuDNN Conv.cpp (the int8    */
+/* convolution computes in INT32; kSpatialDim makes the op generic), and the  */
+/* adjoints of fprop written out above.  The pages give no requantisation    */
+/* for the backward passes, so none is applied.                              */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    oracle_problem pb;
+    int P, Q;
+    const int8_t *A_in, *B_in;
+    const int64_t *idx;
+    int32_t *out;
+    int64_t *acc;
+} int8_back_ctx;
+
+static int32_t oracle_wrap_int32(int64_t v)
+{
+    uint32_t u = (uint32_t)((uint64_t)v & 0xFFFFFFFFu);
+    return u >= 0x80000000u ? (int32_t)(int64_t)(u - 0x100000000LL) : (int32_t)u;
+}
+
+static void dgrad_int8_elem(const void *vctx, int64_t j)
+{
+    const int8_back_ctx *t = (const int8_back_ctx *)vctx;
+    const oracle_problem *p = &t->pb;
+    int64_t e = t->idx ? t->idx[j] : j;
+    int64_t rem = e;
+    int c = (int)(rem % p->C); rem /= p->C;
+    int w = (int)(rem % p->W); rem /= p->W;
+    int h = (int)(rem % p->H); rem /= p->H;
+    int n = (int)rem;
+    int64_t sum = 0;
+    for (int r = 0; r < p->R; ++r) {
+        int th = h + p->pad_h - r * p->dil_h;
+        if (th < 0 || th % p->stride_h != 0) continue;
+        int pp = th / p->stride_h;
+        if (pp >= t->P) continue;
+        for (int s = 0; s < p->S; ++s) {
+            int tw = w + p->pad_w - s * p->dil_w;
+            if (tw < 0 || tw % p->stride_w != 0) continue;
+            int q = tw / p->stride_w;
+            if (q >= t->Q) continue;
+            for (int k = 0; k < p->K; ++k) {
+                int64_t g = t->A_in[(((int64_t)n * t->P + pp) * t->Q + q) * p->K + k];
+                int64_t f = t->B_in[(((int64_t)k * p->R + r) * p->S + s) * p->C + c];
+                sum += g * f;
+            }
+        }
+    }
+    if (t->acc) t->acc[j] = sum;
+    t->out[j] = oracle_wrap_int32(sum);
+}
+
+static void wgrad_int8_elem(const void *vctx, int64_t j)
+{
+    const int8_back_ctx *t = (const int8_back_ctx *)vctx;
+    const oracle_problem *p = &t->pb;
+    int64_t e = t->idx ? t->idx[j] : j;
+    int64_t rem = e;
+    int c = (int)(rem % p->C); rem /= p->C;
+    int s = (int)(rem % p->S); rem /= p->S;
+    int r = (int)(rem % p->R); rem /= p->R;
+    int k = (int)rem;
+    int64_t sum = 0;
+    for (int n = 0; n < p->N; ++n) {
+        for (int pp = 0; pp < t->P; ++pp) {
+            int h = pp * p->stride_h - p->pad_h + r * p->dil_h;
+            if (h < 0 || h >= p->H) continue;
+            for (int q = 0; q < t->Q; ++q) {
+                int w = q * p->stride_w - p->pad_w + s * p->dil_w;
+                if (w < 0 || w >= p->W) continue;
+                int64_t x = t->A_in[(((int64_t)n * p->H + h) * p->W + w) * p->C + c];
+                int64_t g = t->B_in[(((int64_t)n * t->P + pp) * t->Q + q) * p->K + k];
+                sum += g * x;
+            }
+        }
+    }
+    if (t->acc) t->acc[j] = sum;
+    t->out[j] = oracle_wrap_int32(sum);
+}
+
+/* which: 1 dgrad (A_in = dY, B_in = W, idx into [N][H][W][C]),
+ *        2 wgrad (A_in = X, B_in = dY, idx into [K][R][S][C]).
+ * out receives the int32 results; acc (may be NULL) the exact int64 sums. */
+int oracle_backward_int8(int which, const oracle_problem *pb, const int8_t *A_in,
+                         const int8_t *B_in, const int64_t *idx, int64_t count, int32_t *out,
+                         int64_t *acc, int nthreads)
+{
+    int8_back_ctx t;
+    t.pb = *pb;
+    t.P = oracle_out_size(pb->H, pb->pad_h, pb->dil_h, pb->R, pb->stride_h);
+    t.Q = oracle_out_size(pb->W, pb->pad_w, pb->dil_w, pb->S, pb->stride_w);
+    if (t.P <= 0 || t.Q <= 0) return -1;
+    if (which != 1 && which != 2) return -2;
+    t.A_in = A_in; t.B_in = B_in;
+    t.idx = idx; t.out = out; t.acc = acc;
+    oracle_parallel(which == 1 ? dgrad_int8_elem : wgrad_int8_elem, &t, count, nthreads);
     return 0;
 }
 

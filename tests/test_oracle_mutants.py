@@ -12,6 +12,7 @@ import oracle as oracle_mod
 from tests import test_oracle_3d_pins as pins3d
 from tests import test_oracle_abs_pins as apins
 from tests import test_oracle_grouped_pins as gpins
+from tests import test_oracle_int8_back_pins as i8pins
 from tests import test_oracle_pins as pins
 
 SRC = os.path.join(os.path.dirname(oracle_mod.__file__), "conv_oracle.c")
@@ -68,6 +69,19 @@ MUTANTS = [
      "if (td < 0) continue;", 0),
     ("3d wgrad depth dilation dropped", "int d = o * p->stride_d - p->pad_d + tt * p->dil_d;",
      "int d = o * p->stride_d - p->pad_d + tt;", 1),
+    ("int8 dgrad flipped tap", "int th = h + p->pad_h - r * p->dil_h;",
+     "int th = h + p->pad_h - (p->R - 1 - r) * p->dil_h;", 3),
+    ("int8 dgrad stride test dropped", "if (th < 0 || th % p->stride_h != 0) continue;",
+     "if (th < 0) continue;", 3),
+    ("int8 wgrad dilation dropped", "int w = q * p->stride_w - p->pad_w + s * p->dil_w;",
+     "int w = q * p->stride_w - p->pad_w + s;", 7),
+    ("int8 backward saturates instead of wrapping",
+     "uint32_t u = (uint32_t)((uint64_t)v & 0xFFFFFFFFu);",
+     "if (v > 2147483647LL) v = 2147483647LL; if (v < -2147483647LL - 1) v = -2147483647LL - 1;"
+     " uint32_t u = (uint32_t)((uint64_t)v & 0xFFFFFFFFu);", 0),
+    ("int8 wgrad reads X at the dY channel",
+     "int64_t x = t->A_in[(((int64_t)n * p->H + h) * p->W + w) * p->C + c];",
+     "int64_t x = t->A_in[(((int64_t)n * p->H + h) * p->W + w) * p->C + k % p->C];", 0),
     ("permute swaps h and w", "int64_t di = (((int64_t)n * H + h) * W + w) * C + c;\n                    memcpy",
      "int64_t di = (((int64_t)n * W + w) * H + h) * C + c;\n                    memcpy", 0),
 ]
@@ -141,7 +155,11 @@ PIN_CALLS = [
   + [(apins.test_grouped_abs_sums_are_torch_convs_of_magnitudes, {"pb": pb, "groups": g})
      for pb, g in gpins.GROUPED_PROBLEMS] \
   + [(apins.test_3d_abs_sums_are_torch_convs_of_magnitudes, {"pb": pb})
-     for pb in pins3d.PROBLEMS_3D]
+     for pb in pins3d.PROBLEMS_3D] \
+  + [(fn, {"pb": pb}) for pb in i8pins.PROBLEMS
+     for fn in (i8pins.test_int8_backward_equals_fp64_passes,
+                i8pins.test_int8_backward_adjoint_identities_exact)] \
+  + [(i8pins.test_int8_wgrad_wraps_past_2_31, {}), (i8pins.test_int8_dgrad_wraps_past_2_31, {})]
 
 
 def _first_failing_pin():
