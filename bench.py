@@ -658,8 +658,25 @@ def measure_rows(args, device, stream):
     fn = lambda: igc.conv2d_fprop_int8(pb, X, Wt, b, Y, wl["act_scale"], wl["w_scale"],  # noqa
                                        wl["out_scale"], True, ws, need)
     ms = time_call(fn, stream, flush=flush)
-    rows["int8_56x56_128to128_3x3"] = {"TOPS": conv_flops(pb, P, Q) / (ms * 1e-3) / 1e12,
-                                       "ms": ms, "includes": "int8->fp16 widening + GEMM"}
+    r8 = {"fprop": {"TOPS": conv_flops(pb, P, Q) / (ms * 1e-3) / 1e12, "ms": ms,
+                    "includes": "int8->fp16 widening + GEMM"}}
+    # int8 data and weight gradients of the same layer (int32 results)
+    dY8 = inp["dY"].to(device)
+    dX8 = torch.empty((pb["N"], pb["H"], pb["W"], pb["C"]), dtype=torch.int32, device=device)
+    dW8 = torch.empty((pb["K"], pb["R"], pb["S"], pb["C"]), dtype=torch.int32, device=device)
+    del ws
+    for kind, need_fn, call in (
+            ("dgrad", igc.conv2d_dgrad_int8_workspace_size,
+             lambda w8: igc.conv2d_dgrad_int8(pb, dY8, Wt, dX8, w8)),
+            ("wgrad", igc.conv2d_wgrad_int8_workspace_size,
+             lambda w8: igc.conv2d_wgrad_int8(pb, X, dY8, dW8, w8))):
+        w8 = torch.empty(need_fn(pb), dtype=torch.uint8, device=device)
+        ms = time_call(lambda: call(w8), stream, flush=flush)
+        r8[kind] = {"TOPS": conv_flops(pb, P, Q) / (ms * 1e-3) / 1e12, "ms": ms,
+                    "includes": "int8->fp16 widening + GEMM" +
+                                (" + int32 split reduction" if kind == "wgrad" else "")}
+        del w8
+    rows["int8_56x56_128to128_3x3"] = r8
     return rows
 
 

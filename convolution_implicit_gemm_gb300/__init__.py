@@ -24,6 +24,8 @@ __all__ = [
     "conv2d_output_size", "conv2d_fprop", "conv2d_fprop_workspace_size", "conv2d_fprop_ws",
     "conv2d_dgrad", "conv2d_wgrad_workspace_size",
     "conv2d_wgrad", "conv2d_fprop_int8_workspace_size", "conv2d_fprop_int8",
+    "conv2d_dgrad_int8_workspace_size", "conv2d_dgrad_int8", "conv2d_wgrad_int8_workspace_size",
+    "conv2d_wgrad_int8",
     "conv2d_grouped_fprop", "conv2d_grouped_fprop_workspace_size", "conv2d_grouped_fprop_ws",
     "conv2d_grouped_dgrad", "conv2d_grouped_dgrad_workspace_size", "conv2d_grouped_dgrad_ws",
     "conv2d_grouped_wgrad_workspace_size",
@@ -115,6 +117,10 @@ def load():
             "conv2d_wgrad": (I, [PP, I, I, P, P, P, P, F, F, P, SZ, P]),
             "conv2d_fprop_int8_workspace_size": (SZ, [PP]),
             "conv2d_fprop_int8": (I, [PP, P, P, P, P, D, D, D, I, P, SZ, P]),
+            "conv2d_dgrad_int8_workspace_size": (SZ, [PP]),
+            "conv2d_dgrad_int8": (I, [PP, P, P, P, P, SZ, P]),
+            "conv2d_wgrad_int8_workspace_size": (SZ, [PP]),
+            "conv2d_wgrad_int8": (I, [PP, P, P, P, P, SZ, P]),
             "conv2d_grouped_fprop": (I, [PP, I, I, P, P, P, P, P, F, F, I, P]),
             "conv2d_grouped_fprop_workspace_size": (SZ, [PP, I, I]),
             "conv2d_grouped_fprop_ws": (I, [PP, I, I, P, P, P, P, P, F, F, I, P, SZ, P]),
@@ -291,6 +297,42 @@ def conv2d_fprop_int8(prob, X, Wt, bias, Y, act_scale, w_scale, out_scale, relu=
                                     int(bool(relu)), _ptr(workspace), int(workspace_bytes),
                                     _stream(stream)),
            "conv2d_fprop_int8")
+
+
+def conv2d_dgrad_int8_workspace_size(prob) -> int:
+    pb = Problem.make(prob)
+    return int(load().conv2d_dgrad_int8_workspace_size(ctypes.byref(pb)))
+
+
+def conv2d_dgrad_int8(prob, dY, Wt, dX, workspace=None, workspace_bytes=None, stream=None):
+    pb = Problem.make(prob)
+    P, Q = conv2d_output_size(pb)
+    _expect(dY, pb.N * P * Q * pb.K, "dY")
+    _expect(Wt, pb.K * pb.R * pb.S * pb.C, "Wt")
+    _expect(dX, pb.N * pb.H * pb.W * pb.C, "dX")
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().conv2d_dgrad_int8(ctypes.byref(pb), _ptr(dY), _ptr(Wt), _ptr(dX),
+                                    _ptr(workspace), int(workspace_bytes), _stream(stream)),
+           "conv2d_dgrad_int8")
+
+
+def conv2d_wgrad_int8_workspace_size(prob) -> int:
+    pb = Problem.make(prob)
+    return int(load().conv2d_wgrad_int8_workspace_size(ctypes.byref(pb)))
+
+
+def conv2d_wgrad_int8(prob, X, dY, dW, workspace=None, workspace_bytes=None, stream=None):
+    pb = Problem.make(prob)
+    P, Q = conv2d_output_size(pb)
+    _expect(X, pb.N * pb.H * pb.W * pb.C, "X")
+    _expect(dY, pb.N * P * Q * pb.K, "dY")
+    _expect(dW, pb.K * pb.R * pb.S * pb.C, "dW")
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().conv2d_wgrad_int8(ctypes.byref(pb), _ptr(X), _ptr(dY), _ptr(dW),
+                                    _ptr(workspace), int(workspace_bytes), _stream(stream)),
+           "conv2d_wgrad_int8")
 
 
 def _group_sizes(pb, groups):

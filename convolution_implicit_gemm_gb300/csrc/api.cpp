@@ -856,6 +856,51 @@ size_t dw_wgrad_ws_bytes(const DwParams& p) {
 // ===========================================================================
 // C ABI
 // ===========================================================================
+namespace {
+
+// int8 dgrad / wgrad planning helpers
+
+int current_sm_count() {
+  int sm_count = 148;
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+      sm_count = v;
+  } else {
+    cudaGetLastError();  // no device: size for the default SM count
+  }
+  return sm_count;
+}
+
+// Accumulators for a tile whose units have at most max_kb reduction blocks:
+// NI issuers, groups of at most 16 blocks per issuer; false when two TMEM
+// buffers of them do not fit in the 512 columns.
+bool int_accumulators(int bn, int max_kb, int* num_acc, int* kb_per_acc) {
+  const int ni = issuers_for(bn);
+  const int per_issuer = ceil_div(max_kb > 0 ? max_kb : 1, ni);
+  const int groups = ceil_div(per_issuer, 16);
+  if (2 * ni * groups * bn > 512) return false;
+  *num_acc = ni * groups;
+  *kb_per_acc = ceil_div(per_issuer, groups);
+  return true;
+}
+
+// wgrad plan of the int8 path: the fp16 plan, with the split count raised
+// until every split's reduction fits the accumulators of its tile width.
+void plan_wgrad_int8(const igconv_problem_t* pb, int P, int Q, int sm_count, WgradPlan* w) {
+  plan_wgrad_shape(pb, P, Q, sm_count, w);
+  const int ni = issuers_for(w->bn);
+  const int max_groups = 512 / (2 * ni * w->bn);
+  const int max_kb = ni * (max_groups < 1 ? 1 : max_groups) * 16;
+  const int need = ceil_div(w->kblocks, max_kb);
+  if (w->splits < need) w->splits = need;
+  if (w->splits > w->kblocks) w->splits = w->kblocks;
+  w->ws_bytes = static_cast<size_t>(w->splits) * w->M_pad * w->N_pad * sizeof(int32_t);
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* igconv_status_string(igconv_status_t s) {
@@ -1977,6 +2022,157 @@ igconv_status_t conv2d_fprop_int8(const igconv_problem_t* prob, const int8_t* X,
   e = launch_i8_to_f16(Wt, Wh, wcount, s);
   if (e != cudaSuccess) return IGCONV_ERR_CUDA;
   return from_cuda(launch_conv_gemm(p, bn, grid_for(p.units, dev), s));
+}
+
+// ---------------------------------------------------------------------------
+// int8 dgrad / wgrad: int8 operands widened to fp16 copies in the workspace
+// (exact), the dgrad / wgrad implicit GEMM on the fp16 tensor core with each
+// TMEM accumulator summing at most 16 reduction blocks (1024 products of
+// magnitude <= 2^14, so every partial sum is an integer below 2^24, exact in
+// fp32), and the accumulators added as int32 (modulo 2^32) by the epilogue.
+// ---------------------------------------------------------------------------
+size_t conv2d_dgrad_int8_workspace_size(const igconv_problem_t* prob) {
+  int P = 0, Q = 0;
+  if (check_shape(prob, &P, &Q) != IGCONV_OK) return 0;
+  return round256(static_cast<size_t>(prob->N) * P * Q * prob->K * 2) +
+         round256(static_cast<size_t>(prob->K) * prob->R * prob->S * prob->C * 2);
+}
+
+igconv_status_t conv2d_dgrad_int8(const igconv_problem_t* prob, const int8_t* dY,
+                                  const int8_t* Wt, int32_t* dX, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  int P = 0, Q = 0;
+  igconv_status_t st = check_shape(prob, &P, &Q);
+  if (st != IGCONV_OK) return st;
+  if (!dY || !Wt || !dX) return IGCONV_ERR_INVALID_ARG;
+  if ((st = check_limits(prob, P, Q, 16)) != IGCONV_OK) return st;
+  if (prob->stride_h * prob->stride_w > kMaxSub) return IGCONV_ERR_UNSUPPORTED;
+  if (!aligned16(dY) || !aligned16(Wt) || !aligned16(dX) || (workspace && !aligned16(workspace)))
+    return IGCONV_ERR_MISALIGNED;
+  const size_t need = conv2d_dgrad_int8_workspace_size(prob);
+  if (!workspace || workspace_bytes < need) return IGCONV_ERR_WORKSPACE;
+  DeviceState* dev = nullptr;
+  if ((st = device_state(&dev)) != IGCONV_OK) return st;
+  const long long ycount = static_cast<long long>(prob->N) * P * Q * prob->K;
+  const long long wcount = static_cast<long long>(prob->K) * prob->R * prob->S * prob->C;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* dYh = ws;
+  void* Wh = ws + round256(static_cast<size_t>(ycount) * 2);
+  ConvGemmParams p;
+  int bn = 0, forced = g_tune_bn.load();
+  for (;;) {
+    init_common(p, dev);
+    if ((st = plan_dgrad(p, &bn, prob, P, Q, 0, dYh, Wh, dev->sm_count, forced)) != IGCONV_OK)
+      return st;
+    int max_kb = 0;
+    for (int i = 0; i < p.nsub; ++i) {
+      const int kb = p.sub[i].rcount * p.sub[i].scount * p.cblocks;
+      if (kb > max_kb) max_kb = kb;
+    }
+    if (int_accumulators(bn, max_kb, &p.num_acc, &p.kb_per_acc)) break;
+    if (bn == 64 || forced) return IGCONV_ERR_UNSUPPORTED;
+    forced = bn >> 1;
+  }
+  p.epi = EPI_STORE;
+  p.int_acc = 1;
+  p.out = dX;
+  p.use_tma_store = 0;
+  p.alpha = 1.0f;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_i8_to_f16(dY, dYh, ycount, s);
+  if (e != cudaSuccess) return IGCONV_ERR_CUDA;
+  e = launch_i8_to_f16(Wt, Wh, wcount, s);
+  if (e != cudaSuccess) return IGCONV_ERR_CUDA;
+  if (p.units == 0) return IGCONV_OK;
+  return from_cuda(launch_conv_gemm(p, bn, grid_for(p.units, dev), s));
+}
+
+size_t conv2d_wgrad_int8_workspace_size(const igconv_problem_t* prob) {
+  int P = 0, Q = 0;
+  if (check_shape(prob, &P, &Q) != IGCONV_OK) return 0;
+  WgradPlan w;
+  plan_wgrad_int8(prob, P, Q, current_sm_count(), &w);
+  return round256(static_cast<size_t>(prob->N) * prob->H * prob->W * prob->C * 2) +
+         round256(static_cast<size_t>(prob->N) * P * Q * prob->K * 2) + round256(w.ws_bytes);
+}
+
+igconv_status_t conv2d_wgrad_int8(const igconv_problem_t* prob, const int8_t* X, const int8_t* dY,
+                                  int32_t* dW, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
+  int P = 0, Q = 0;
+  igconv_status_t st = check_shape(prob, &P, &Q);
+  if (st != IGCONV_OK) return st;
+  if (!X || !dY || !dW) return IGCONV_ERR_INVALID_ARG;
+  if ((st = check_limits(prob, P, Q, 16)) != IGCONV_OK) return st;
+  if (!aligned16(X) || !aligned16(dY) || !aligned16(dW) || (workspace && !aligned16(workspace)))
+    return IGCONV_ERR_MISALIGNED;
+  DeviceState* dev = nullptr;
+  if ((st = device_state(&dev)) != IGCONV_OK) return st;
+  WgradPlan w;
+  plan_wgrad_int8(prob, P, Q, dev->sm_count, &w);
+  const long long xcount = static_cast<long long>(prob->N) * prob->H * prob->W * prob->C;
+  const long long npq = static_cast<long long>(prob->N) * P * Q;
+  const long long ycount = npq * prob->K;
+  const size_t xb = round256(static_cast<size_t>(xcount) * 2);
+  const size_t yb = round256(static_cast<size_t>(ycount) * 2);
+  if (!workspace || workspace_bytes < xb + yb + round256(w.ws_bytes)) return IGCONV_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* Xh = ws;
+  void* dYh = ws + xb;
+  void* part = ws + xb + yb;
+  ConvGemmParams p;
+  init_common(p, dev);
+  p.nsub = 1;
+  p.a_src = w.swapped ? SRC_2D_MN : SRC_IM2COL_MN;
+  p.b_src = w.swapped ? SRC_IM2COL_MN : SRC_2D_MN;
+  p.epi = EPI_PARTIAL;
+  p.int_acc = 1;
+  p.tiles_m_total = w.tiles_m;
+  p.tiles_n = w.tiles_n;
+  p.splits = w.splits;
+  p.kblocks_total = w.kblocks;
+  p.units = w.tiles_m * w.tiles_n * w.splits;
+  p.cblocks = w.cblocks;
+  p.N_gemm = w.N_pad;
+  p.idesc = make_idesc(kBlockM, w.bn, 0, 1, 1);
+  if (!int_accumulators(w.bn, ceil_div(w.kblocks, w.splits), &p.num_acc, &p.kb_per_acc))
+    return IGCONV_ERR_UNSUPPORTED;  // not reached: the plan sized the splits for this
+  p.wg_PQ = P * Q;
+  p.wg_Q = Q;
+  p.wg_lower_h = -prob->pad_h;
+  p.wg_lower_w = -prob->pad_w;
+  p.wg_sh = prob->stride_h;
+  p.wg_sw = prob->stride_w;
+  p.wg_S = prob->S;
+  p.wg_RS = w.rs;
+  p.wg_dh = prob->dil_h;
+  p.wg_dw = prob->dil_w;
+  p.wg_K = prob->K;
+  p.out = part;
+  p.ws_split_stride = static_cast<long long>(w.M_pad) * w.N_pad;
+  p.ws_ld = w.N_pad;
+  p.use_tma_store = encode_out_2d(&p.mapY, part, CU_TENSOR_MAP_DATA_TYPE_INT32, 4,
+                                  static_cast<long long>(w.splits) * w.M_pad, w.N_pad, 16,
+                                  CU_TENSOR_MAP_SWIZZLE_64B) ? 1 : 0;
+  if (!encode_im2col(&p.mapA[0], Xh, 0, prob->N, prob->H, prob->W, prob->C, -prob->pad_h,
+                     -prob->pad_w, prob->pad_h - (prob->R - 1) * prob->dil_h,
+                     prob->pad_w - (prob->S - 1) * prob->dil_w, prob->stride_h, prob->stride_w,
+                     kBlockK))
+    return IGCONV_ERR_UNSUPPORTED;
+  p.mapA_valid = 1u;
+  if (!encode_2d(&p.mapB, dYh, 0, npq, prob->K)) return IGCONV_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_i8_to_f16(X, Xh, xcount, s);
+  if (e != cudaSuccess) return IGCONV_ERR_CUDA;
+  e = launch_i8_to_f16(dY, dYh, ycount, s);
+  if (e != cudaSuccess) return IGCONV_ERR_CUDA;
+  e = launch_conv_gemm(p, w.bn, grid_for(p.units, dev), s);
+  if (e != cudaSuccess) return IGCONV_ERR_CUDA;
+  const int xext = w.rs * w.cpad;
+  return from_cuda(launch_wgrad_reduce_i32(static_cast<const int*>(part), w.splits,
+                                           p.ws_split_stride, w.N_pad,
+                                           w.swapped ? prob->K : xext, w.swapped ? xext : prob->K,
+                                           w.swapped, prob->K, w.rs, prob->C, w.cpad, dW, s));
 }
 
 igconv_status_t nchw_to_nhwc(const void* src, void* dst, int N, int C, int H, int W,

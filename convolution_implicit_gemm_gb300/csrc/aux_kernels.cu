@@ -1,6 +1,6 @@
 // aux_kernels.cu -- the bandwidth-bound kernels around the implicit GEMM:
 //   * batched transpose for the NCHW <-> NHWC permutes
-//   * the deterministic split-K reduction of wgrad
+//   * the deterministic split-K reduction of wgrad (fp32, and int32 for int8)
 //   * int8 -> fp16 widening of the int8 operands
 //   * the per-device status word and the wait-timeout self-test
 #include <cuda_bf16.h>
@@ -510,6 +510,47 @@ cudaError_t launch_wgrad_reduce(const float* ws, int splits, long long split_str
     default: IGC_REDUCE(1); break;
   }
 #undef IGC_REDUCE
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// int8 wgrad: dW[k][rs][c] (int32) = the int32 partial tiles of the splits
+// added in split order, wrapping modulo 2^32 like the int32 accumulator they
+// stand for.  One thread per element of the partial matrix, so the reads of
+// every split run along its rows; rows past the valid extent are skipped.
+//   not swapped: rows (tap, c) over rs * cpad, columns k
+//   swapped:     rows k, columns (tap, c)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) wgrad_reduce_i32_kernel(
+    const int* __restrict__ ws, int splits, long long split_stride, int ws_ld, int rows, int cols,
+    int swapped, int K, int RS, int C, int cpad, int* __restrict__ dW) {
+  const long long total = static_cast<long long>(rows) * cols;
+  for (long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
+       e += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int m = static_cast<int>(e / cols);
+    const int n = static_cast<int>(e - static_cast<long long>(m) * cols);
+    const int k = swapped ? m : n;
+    const int x = swapped ? n : m;
+    const int rs = x / cpad;
+    const int c = x - rs * cpad;
+    if (k >= K || rs >= RS || c >= C) continue;
+    const int* src = ws + static_cast<long long>(m) * ws_ld + n;
+    uint32_t sum = 0u;
+    for (int sp = 0; sp < splits; ++sp)
+      sum += static_cast<uint32_t>(src[static_cast<long long>(sp) * split_stride]);
+    dW[(static_cast<long long>(k) * RS + rs) * C + c] = static_cast<int>(sum);
+  }
+}
+
+cudaError_t launch_wgrad_reduce_i32(const int* ws, int splits, long long split_stride, int ws_ld,
+                                    int rows, int cols, int swapped, int K, int RS, int C,
+                                    int cpad, int* dW, cudaStream_t s) {
+  const long long total = static_cast<long long>(rows) * cols;
+  long long blocks = (total + 255) / 256;
+  if (blocks < 1) blocks = 1;
+  if (blocks > 16384) blocks = 16384;
+  wgrad_reduce_i32_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+      ws, splits, split_stride, ws_ld, rows, cols, swapped, K, RS, C, cpad, dW);
   return cudaGetLastError();
 }
 

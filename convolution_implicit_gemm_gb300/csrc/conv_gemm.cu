@@ -837,6 +837,27 @@ __device__ __forceinline__ bool acc_used(int kb_per_acc, int a, int ni, int nk, 
   return static_cast<long long>(grp) * kb_per_acc * ni + first_rel(a % ni, ni, q0) < nk;
 }
 
+// Integer sum of the used accumulators of 32 columns (chunk at column
+// offset col of each accumulator): each holds an exact integer below 2^24 in
+// magnitude, converted exactly; the adds wrap modulo 2^32 like an int32
+// accumulator.
+__device__ __forceinline__ void int_acc_sum(uint32_t t_row, uint32_t col, int num_acc, int bn,
+                                            int kb_per_acc, int ni, int nk, int q0,
+                                            int (&iacc)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) iacc[i] = 0;
+  for (int a = 0; a < num_acc; ++a) {
+    if (!acc_used(kb_per_acc, a, ni, nk, q0)) continue;
+    uint32_t v[32];
+    tmem_ld_32x32b_x32(t_row + a * bn + col, v);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      iacc[i] = static_cast<int>(static_cast<uint32_t>(iacc[i]) +
+                                 static_cast<uint32_t>(__float2int_rn(__uint_as_float(v[i]))));
+  }
+}
+
 // Epilogue scalars, copied into registers once.
 struct EpiCtx {
   Sched sc;
@@ -854,6 +875,7 @@ struct EpiCtx {
   int use_tma;
   int box64;            // 16-bit output boxes of 64 columns (128-byte swizzle)
   int ws_rows_per_split;   // M_pad (wgrad)
+  int int_acc;             // accumulators hold exact integers: sum and store them as int32
   const CUtensorMap* mapY;
 };
 
@@ -887,6 +909,7 @@ __device__ __forceinline__ void run_epilogue(const ConvGemmParams& p, uint64_t* 
   e.use_tma = p.use_tma_store;
   e.box64 = p.use_tma_store && p.store_box64 && e.sc.epi == EPI_STORE;
   e.ws_rows_per_split = p.tiles_m_total * kBlockM;
+  e.int_acc = p.int_acc;
   e.mapY = &p.mapY;
   // bias_s holds the whole bias vector when it fits in kBiasBytes (fp32 for
   // the 16-bit passes, int32 for int8); every lane reads the same entries,
@@ -952,6 +975,17 @@ __device__ __forceinline__ void run_epilogue(const ConvGemmParams& p, uint64_t* 
       };
 #pragma unroll 1
       for (int j = j0; j < j1; ++j) {
+        if (e.int_acc) {
+          // int8 wgrad: the int32 sum of the accumulators, stored as its bits
+          int iacc[32];
+          int_acc_sum(t_row, static_cast<uint32_t>(j * 32), e.num_acc, BN, e.kb_per_acc, NI, nk,
+                      q0, iacc);
+          float acc[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[i] = __int_as_float(iacc[i]);
+          store_partial(acc, j);
+          continue;
+        }
         if (NI == 1 && e.num_acc == 1 && j + 1 < j1) {
           // one accumulator: two chunks per TMEM round trip
           uint32_t v[32], u2[32];
@@ -1035,6 +1069,27 @@ __device__ __forceinline__ void run_epilogue(const ConvGemmParams& p, uint64_t* 
         const int n0 = w.tile_n * BN + j * 32;
         if (n0 >= e.N_gemm) break;  // warp-uniform
         const int ncols = min(32, e.N_gemm - n0);
+        if (e.int_acc) {
+          // int8 dgrad: the exact int32 sum, written as two 16-column rows
+          // of 64 bytes (the column count is a multiple of 16)
+          int iacc[32];
+          int_acc_sum(t_row, static_cast<uint32_t>(j * 32), e.num_acc, BN, e.kb_per_acc, NI, nk,
+                      q0, iacc);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            if (16 * h >= ncols) break;  // warp-uniform
+            const uint4 o[4] = {
+                make_uint4(iacc[16 * h], iacc[16 * h + 1], iacc[16 * h + 2], iacc[16 * h + 3]),
+                make_uint4(iacc[16 * h + 4], iacc[16 * h + 5], iacc[16 * h + 6], iacc[16 * h + 7]),
+                make_uint4(iacc[16 * h + 8], iacc[16 * h + 9], iacc[16 * h + 10], iacc[16 * h + 11]),
+                make_uint4(iacc[16 * h + 12], iacc[16 * h + 13], iacc[16 * h + 14],
+                           iacc[16 * h + 15])};
+            warp_store_rows(stage, o, 4, valid ? row_off * 4 : -1LL,
+                            static_cast<uint8_t*>(e.out) + static_cast<long long>(n0 + 16 * h) * 4,
+                            lane);
+          }
+          continue;
+        }
         if (e.sc.epi == EPI_INT8) {
           int iacc[32];
 #pragma unroll

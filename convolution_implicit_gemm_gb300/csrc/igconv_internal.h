@@ -122,6 +122,9 @@ struct ConvGemmParams {
   int ws_ld;                  // wgrad: padded N extent
   uint32_t rq_mant;           // int8: multiplier M = rq_mant * 2^rq_exp exactly
   int rq_exp;
+  int int_acc;                // 1: the accumulators hold exact integers (int8 operands on the
+                              // fp16 path); EPI_STORE writes their int32 sum, EPI_PARTIAL
+                              // int32 partial sums (int8 dgrad / wgrad)
   unsigned int* status;       // device status word
   unsigned long long timeout_ns;
 };
@@ -139,6 +142,9 @@ cudaError_t launch_wgrad_reduce(const float* ws, int splits, long long split_str
                                 int rows, int cols, int swapped, int K, int RS, int C, int cpad,
                                 void* dW, int dw_dtype, const void* cin, float alpha, float beta,
                                 cudaStream_t s);
+cudaError_t launch_wgrad_reduce_i32(const int* ws, int splits, long long split_stride, int ws_ld,
+                                    int rows, int cols, int swapped, int K, int RS, int C,
+                                    int cpad, int* dW, cudaStream_t s);
 cudaError_t launch_i8_to_f16(const int8_t* src, void* dst, long long count, cudaStream_t s);
 cudaError_t launch_pad_pixels8(const void* src, void* dst, long long pixels, int C,
                                cudaStream_t s);

@@ -411,6 +411,37 @@ IGCONV_API igconv_status_t conv2d_fprop_int8(const igconv_problem_t *prob, const
                                              int relu, void *workspace, size_t workspace_bytes,
                                              void *stream);
 
+/* int8 data and weight gradients, int32 results (the int8 convolution's
+ * INT32 compute type of PyTorch quantized cuDNN Conv.cpp, whose op is generic
+ * over the spatial rank, carried to the adjoint passes of conv2d_dgrad and
+ * conv2d_wgrad).  The pages define no requantisation for these passes, so
+ * the result is the integer sum itself, delivered as int32: the exact sum
+ * modulo 2^32 (two's complement), what an int32 accumulator holds.
+ *   dX[n,h,w,c] = sum over (k, r, s) and the output position (p, q) that
+ *                 reads (h, w) through tap (r, s) of dY[n,p,q,k] * Wt[k,r,s,c]
+ *   dW[k,r,s,c] = sum_{n,p,q} dY[n,p,q,k] * X[n, p*sh - ph + r*dh, q*sw - pw + s*dw, c]
+ * The operands are widened to fp16 copies in the workspace (exact); the
+ * implicit GEMM of the 16-bit pass runs on them with every fp32 accumulator
+ * summing at most 1024 products (each partial sum an integer below 2^24, so
+ * exact), and the epilogue adds the accumulators as int32.  Input positions
+ * no output reads get 0.
+ *   dY [N][P][Q][K] int8, X [N][H][W][C] int8, Wt [K][R][S][C] int8,
+ *   dX [N][H][W][C] int32 (written), dW [K][R][S][C] int32 (written).
+ *   C and K multiples of 16; dgrad: stride_h * stride_w <= 16; dgrad and
+ *   the per-split reduction must fit the accumulators (else UNSUPPORTED).
+ *   workspace  >= the *_workspace_size() bytes (queried on the current device
+ *              for wgrad), caller-owned, overwritten; not shared with a
+ *              concurrent call.
+ * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, WORKSPACE, CUDA. */
+IGCONV_API size_t conv2d_dgrad_int8_workspace_size(const igconv_problem_t *prob);
+IGCONV_API igconv_status_t conv2d_dgrad_int8(const igconv_problem_t *prob, const int8_t *dY,
+                                             const int8_t *Wt, int32_t *dX, void *workspace,
+                                             size_t workspace_bytes, void *stream);
+IGCONV_API size_t conv2d_wgrad_int8_workspace_size(const igconv_problem_t *prob);
+IGCONV_API igconv_status_t conv2d_wgrad_int8(const igconv_problem_t *prob, const int8_t *X,
+                                             const int8_t *dY, int32_t *dW, void *workspace,
+                                             size_t workspace_bytes, void *stream);
+
 /* Layout permutes (burn-cubecl "kernel/conv/base.rs": permute_nchw_to_nhwc
  * around the NHWC core in `conv_forward`, permute_nhwc_to_nchw after it).
  *   nchw_to_nhwc: dst[n][h][w][c] = src[n][c][h][w]

@@ -158,7 +158,9 @@ def make_inputs(problem: dict, P: int, Q: int, dtype: str, recipe: str, seed: in
       int_uniform  ceil(U(-4.5, 3.5)) for X, W, dY, C; bias integer in [-4, 4]
       normal_he    X, dY ~ N(0, 1); W ~ N(0, 2/(C/groups*R*S)); bias, C ~ N(0, 1)
       normal_w005  X, dY ~ N(0, 1); W ~ N(0, 0.05) (variance); C ~ N(0, 1)
-      int8         X ~ U{-128..127}, W ~ U{-127..127}, bias ~ U[-2^14, 2^14]
+      int8         X ~ U{-128..127}, W ~ U{-127..127}, bias ~ U[-2^14, 2^14], then
+                   dY ~ U{-128..127} (for the int8 gradients; drawn last, so the
+                   forward operands are the same with or without it)
     """
     N, H, W, C, K, R, S = (problem[k] for k in "NHWCKRS")
     Cg = C // groups   # filter channels: the input channels of one group
@@ -172,6 +174,8 @@ def make_inputs(problem: dict, P: int, Q: int, dtype: str, recipe: str, seed: in
         if bias:
             out["bias"] = torch.randint(-(1 << 14), (1 << 14) + 1, (K,), generator=g,
                                         dtype=torch.int32)
+        out["dY"] = _nchw_draw_to_nhwc(
+            torch.randint(-128, 128, (N, K, P, Q), generator=g, dtype=torch.int32).to(torch.int8))
         return out
     td = TORCH_DTYPES[dtype]
     dwd = TORCH_DTYPES[dw_dtype] if dw_dtype else td
