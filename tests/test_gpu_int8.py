@@ -103,3 +103,34 @@ def test_int8_odd_products_near_2_24_are_exact(C, pattern):
     # the oracle agrees on the same inputs (its accumulation is int64)
     ref = oracle.fprop_int8(pb, X.numpy(), Wt.numpy(), bias.numpy(), 1.0, 1.0, 1.0, relu=False)
     np.testing.assert_array_equal(got, ref)
+
+
+@pytest.mark.parametrize("scales", [(1.0, 0.5, 1.0), (1.0, 1.0, 8.0), (0.5, 0.25, 3.0)])
+def test_int8_requant_ties_exact(scales):
+    """Small integer operands and M = 1/2 or 1/8 put many products t * M
+    exactly on half-integers (ties to even) and the rest near them, so the
+    epilogue's exact integer path decides a large share of the outputs;
+    M = 1/24 gives values off the dyadic grid.  Every output must equal the
+    oracle's."""
+    pb = problem(2, 9, 9, 16, 32, 3, 3, (1, 1))
+    P, Q = igc.conv2d_output_size(pb)
+    g = torch.Generator().manual_seed(97)
+    X = torch.randint(-3, 4, (2, 9, 9, 16), generator=g, dtype=torch.int32).to(torch.int8)
+    Wt = torch.randint(-3, 4, (32, 3, 3, 16), generator=g, dtype=torch.int32).to(torch.int8)
+    bias = torch.randint(-40, 41, (32,), generator=g, dtype=torch.int32)
+    for relu in (False, True):
+        got = run_int8(pb, X, Wt, bias, *scales, relu)
+        ref = oracle.fprop_int8(pb, X.numpy(), Wt.numpy(), bias.numpy(), *scales, relu=relu)
+        np.testing.assert_array_equal(got, ref)
+
+
+def test_int8_extreme_bias_is_exact():
+    """int32 biases near the ends of the range: the bias add is exact in 64
+    bits (no wrap), so outputs saturate the way the oracle's int64 sum says."""
+    pb = problem(1, 6, 6, 16, 16, 3, 3, (1, 1))
+    inp, P, Q = inputs(pb, "i8", "int8", 101)
+    bias = torch.tensor([2 ** 31 - 1, -2 ** 31] * 8, dtype=torch.int32)
+    got = run_int8(pb, inp["X"], inp["W"], bias, 0.02, 0.01, 0.05, False)
+    ref = oracle.fprop_int8(pb, inp["X"].numpy(), inp["W"].numpy(), bias.numpy(), 0.02, 0.01,
+                            0.05, relu=False)
+    np.testing.assert_array_equal(got, ref)
