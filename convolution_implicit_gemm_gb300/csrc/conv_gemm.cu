@@ -707,22 +707,19 @@ __device__ __forceinline__ int requant_exact(long long t, uint32_t mant, int exp
   return static_cast<int>(q);
 }
 
-// The same result through fp32 where that is safe, for |t| <= 2^25: yf =
-// fp32(t) * M differs from the exact t * M by at most 2^-17 when |t| <= 2^24
-// (fp32(t) exact, one rounding of a product below 160), and by less than
-// 2^-12 when 2^24 < |t| <= 2^25 and M < 2^-13 (fp32(t) off by at most 1,
-// times M); with M >= 2^-13 such a t gives |t * M| >= 2048, which saturates.  So when yf is not within 2^-12 of
-// a half-integer, rounding yf gives the rounding of t * M; otherwise (about
-// one value in 2048) the integer path decides.  M = mf = mant * 2^exp.
-__device__ __forceinline__ int requant_fast(int t, float mf, uint32_t mant, int exp) {
-  const float yf = __fmul_rn(__int2float_rn(t), mf);
-  if (fabsf(yf) >= 160.0f) return yf > 0.0f ? 127 : -128;
-  const float frac = yf - floorf(yf);
-  if (fabsf(frac - 0.5f) > 0.000244140625f) {  // 2^-12
-    const int q = __float2int_rn(yf);
-    return q > 127 ? 127 : (q < -128 ? -128 : q);
-  }
-  return requant_exact(static_cast<long long>(t), mant, exp);
+// round_half_even(t * M) clamped to int8 without branches, for M = mant *
+// 2^-sh with 1 <= sh <= 62 and |t| < 2^33: with x = t * mant (exact in 64
+// bits) and b the lowest bit of floor(x / 2^sh), the quotient
+// floor((x + b + 2^(sh-1) - 1) / 2^sh) rounds x / 2^sh to nearest with ties to
+// the even neighbour (an arithmetic shift is the floor, also for negative x).
+__device__ __forceinline__ int requant_rne(long long t, uint32_t mant, int sh,
+                                          long long half_m1) {
+  const long long x = t * static_cast<long long>(mant);
+  const long long b = (x >> sh) & 1LL;
+  long long q = (x + b + half_m1) >> sh;
+  q = q > 127 ? 127 : q;
+  q = q < -128 ? -128 : q;
+  return static_cast<int>(q);
 }
 
 // Writes 32 staged rows to global memory with coalesced 16-byte stores.
@@ -933,8 +930,11 @@ __device__ __forceinline__ void run_epilogue(const ConvGemmParams& p, uint64_t* 
   // the 16-bit passes, int32 for int8); every lane reads the same entries,
   // so the reads are shared-memory broadcasts.
   const bool bias_cached = p.bias_cached != 0;
-  // the int8 multiplier as fp32 (exact: a 24-bit significand times 2^rq_exp)
-  const float rq_mf = ldexpf(static_cast<float>(e.rq_mant), e.rq_exp);
+  // int8 multiplier M = rq_mant * 2^-rq_sh; shifts of 1..62 take the
+  // branch-free rounding (every M of practical size: 2^-38 < M < 2^23)
+  const int rq_sh = -e.rq_exp;
+  const bool rq_plain = rq_sh >= 1 && rq_sh <= 62;
+  const long long rq_half_m1 = rq_plain ? (1LL << (rq_sh - 1)) - 1 : 0;
 
   const int quarter = warp & 3;
   const int half = (warp - kEpiWarp0) >> 2;   // which half of the tile's columns
@@ -1136,12 +1136,11 @@ __device__ __forceinline__ void run_epilogue(const ConvGemmParams& p, uint64_t* 
           for (int i = 0; i < 8; ++i) packed[i] = 0u;
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            // |acc| <= 4096 * 2^14 = 2^26; the bias add is exact in 64 bits
+            // |acc| <= 4096 * 2^14 = 2^26, so |t| < 2^32: exact in 64 bits
             long long t = static_cast<long long>(iacc[i]) + bv[i];
             if (e.relu && t < 0) t = 0;
-            const int y = (t >= -(1LL << 25) && t <= (1LL << 25))
-                              ? requant_fast(static_cast<int>(t), rq_mf, e.rq_mant, e.rq_exp)
-                              : requant_exact(t, e.rq_mant, e.rq_exp);
+            const int y = rq_plain ? requant_rne(t, e.rq_mant, rq_sh, rq_half_m1)
+                                   : requant_exact(t, e.rq_mant, e.rq_exp);
             packed[i >> 2] |= (static_cast<uint32_t>(y) & 0xFFu) << (8 * (i & 3));
           }
           const uint4 o[2] = {make_uint4(packed[0], packed[1], packed[2], packed[3]),
