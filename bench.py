@@ -646,6 +646,21 @@ def measure_rows(args, device, stream):
         r3[kind] = {"TFLOP/s": fl3 / (ms * 1e-3) / 1e12, "ms": ms}
     rows["r3d_16x56x56_64to64_3x3x3"] = r3
     del X3, W3, b3, Y3, dY3, dX3, dW3, ws3
+    # Winograd F(2x2, 3x3) forward of the 56x56 64->64 3x3 layer (direct-sum
+    # FLOPs over time, so the rate compares with the implicit GEMM's)
+    L = Layer("resnet50_56x56_64to64_3x3", device=device)
+    need_w = igc.conv2d_fprop_winograd_workspace_size(L.pb, L.td)
+    ws_w = torch.empty(need_w, dtype=torch.uint8, device=device)
+    ms_w = time_call(lambda: igc.conv2d_fprop_winograd(L.pb, L.td, L.X, L.W, L.b, None, L.Y, 1.0,
+                                                       0.0, L.relu, ws_w), stream, flush=flush)
+    ms_g = time_call(L.fprop, stream, flush=flush)
+    rows["winograd_f2x2_3x3_56x56_64to64"] = {
+        "winograd": {"TFLOP/s": L.flops / (ms_w * 1e-3) / 1e12, "ms": ms_w,
+                     "workspace_MB": need_w / 1e6,
+                     "includes": "input and filter transforms, 16 transform-domain GEMMs "
+                                 "(one launch), output transform"},
+        "implicit_gemm": {"TFLOP/s": L.flops / (ms_g * 1e-3) / 1e12, "ms": ms_g}}
+    del L, ws_w
     # int8 quantised fprop (ops counted like FLOPs: 2 per multiply-add)
     wl = WORKLOADS["int8_56x56_128to128_3x3"]
     pb = wl["problem"]

@@ -25,7 +25,7 @@ __all__ = [
     "conv2d_dgrad", "conv2d_wgrad_workspace_size",
     "conv2d_wgrad", "conv2d_fprop_int8_workspace_size", "conv2d_fprop_int8",
     "conv2d_dgrad_int8_workspace_size", "conv2d_dgrad_int8", "conv2d_wgrad_int8_workspace_size",
-    "conv2d_wgrad_int8",
+    "conv2d_wgrad_int8", "conv2d_fprop_winograd_workspace_size", "conv2d_fprop_winograd",
     "conv2d_grouped_fprop", "conv2d_grouped_fprop_workspace_size", "conv2d_grouped_fprop_ws",
     "conv2d_grouped_dgrad", "conv2d_grouped_dgrad_workspace_size", "conv2d_grouped_dgrad_ws",
     "conv2d_grouped_wgrad_workspace_size",
@@ -117,6 +117,8 @@ def load():
             "conv2d_wgrad": (I, [PP, I, I, P, P, P, P, F, F, P, SZ, P]),
             "conv2d_fprop_int8_workspace_size": (SZ, [PP]),
             "conv2d_fprop_int8": (I, [PP, P, P, P, P, D, D, D, I, P, SZ, P]),
+            "conv2d_fprop_winograd_workspace_size": (SZ, [PP, I]),
+            "conv2d_fprop_winograd": (I, [PP, I, P, P, P, P, P, F, F, I, P, SZ, P]),
             "conv2d_dgrad_int8_workspace_size": (SZ, [PP]),
             "conv2d_dgrad_int8": (I, [PP, P, P, P, P, SZ, P]),
             "conv2d_wgrad_int8_workspace_size": (SZ, [PP]),
@@ -297,6 +299,30 @@ def conv2d_fprop_int8(prob, X, Wt, bias, Y, act_scale, w_scale, out_scale, relu=
                                     int(bool(relu)), _ptr(workspace), int(workspace_bytes),
                                     _stream(stream)),
            "conv2d_fprop_int8")
+
+
+def conv2d_fprop_winograd_workspace_size(prob, dtype) -> int:
+    pb = Problem.make(prob)
+    return int(load().conv2d_fprop_winograd_workspace_size(ctypes.byref(pb), _dtype_code(dtype)))
+
+
+def conv2d_fprop_winograd(prob, dtype, X, Wt, bias, Cin, Y, alpha=1.0, beta=0.0, relu=False,
+                          workspace=None, workspace_bytes=None, stream=None):
+    pb = Problem.make(prob)
+    P, Q = conv2d_output_size(pb)
+    _expect(X, pb.N * pb.H * pb.W * pb.C, "X")
+    _expect(Wt, pb.K * pb.R * pb.S * pb.C, "Wt")
+    _expect(bias, pb.K, "bias")
+    _expect(Y, pb.N * P * Q * pb.K, "Y")
+    if beta != 0.0:
+        _expect(Cin, pb.N * P * Q * pb.K, "Cin")
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().conv2d_fprop_winograd(ctypes.byref(pb), _dtype_code(dtype), _ptr(X), _ptr(Wt),
+                                        _ptr(bias), _ptr(Cin) if beta != 0.0 else None, _ptr(Y),
+                                        float(alpha), float(beta), int(bool(relu)),
+                                        _ptr(workspace), int(workspace_bytes), _stream(stream)),
+           "conv2d_fprop_winograd")
 
 
 def conv2d_dgrad_int8_workspace_size(prob) -> int:

@@ -899,6 +899,32 @@ void plan_wgrad_int8(const igconv_problem_t* pb, int P, int Q, int sm_count, Wgr
   w->ws_bytes = static_cast<size_t>(w->splits) * w->M_pad * w->N_pad * sizeof(int32_t);
 }
 
+// Winograd F(2x2, 3x3): output tiles and workspace parts (V [16][T][C],
+// U [K][16][C], M [16][T][K], all 16-bit).
+struct WinoWs {
+  int TH, TW;
+  long long T;
+  size_t v_bytes, u_bytes, m_bytes, total;
+};
+
+bool wino_ws(const igconv_problem_t* pb, int P, int Q, WinoWs* w) {
+  w->TH = (P + 1) / 2;
+  w->TW = (Q + 1) / 2;
+  w->T = static_cast<long long>(pb->N) * w->TH * w->TW;
+  if (w->T >= (1LL << 31) || w->T * pb->C >= (1LL << 40) || w->T * pb->K >= (1LL << 40))
+    return false;
+  w->v_bytes = round256(static_cast<size_t>(16) * w->T * pb->C * 2);
+  w->u_bytes = round256(static_cast<size_t>(pb->K) * 16 * pb->C * 2);
+  w->m_bytes = round256(static_cast<size_t>(16) * w->T * pb->K * 2);
+  w->total = w->v_bytes + w->u_bytes + w->m_bytes;
+  return true;
+}
+
+bool wino_shape(const igconv_problem_t* pb) {
+  return pb->R == 3 && pb->S == 3 && pb->stride_h == 1 && pb->stride_w == 1 && pb->dil_h == 1 &&
+         pb->dil_w == 1;
+}
+
 }  // namespace
 
 extern "C" {
@@ -2173,6 +2199,104 @@ igconv_status_t conv2d_wgrad_int8(const igconv_problem_t* prob, const int8_t* X,
                                            p.ws_split_stride, w.N_pad,
                                            w.swapped ? prob->K : xext, w.swapped ? xext : prob->K,
                                            w.swapped, prob->K, w.rs, prob->C, w.cpad, dW, s));
+}
+
+// ---------------------------------------------------------------------------
+// Winograd F(2x2, 3x3) forward pass: input and filter transforms on the CUDA
+// cores, the 16 transform-domain GEMMs as one implicit-GEMM launch with one
+// sub-problem per transform point xi (a 1x1 GEMM over V[xi] and filter tap xi
+// of U viewed as [K][16][1][C], written to rows xi of M viewed as a
+// [16][T][K] image), then the output transform with fprop's epilogue.
+// ---------------------------------------------------------------------------
+size_t conv2d_fprop_winograd_workspace_size(const igconv_problem_t* prob, igconv_dtype_t dtype) {
+  int P = 0, Q = 0;
+  if (check_shape(prob, &P, &Q) != IGCONV_OK) return 0;
+  if (dtype != IGCONV_F16 && dtype != IGCONV_BF16) return 0;
+  if (!wino_shape(prob)) return 0;
+  WinoWs w;
+  if (!wino_ws(prob, P, Q, &w)) return 0;
+  return w.total;
+}
+
+igconv_status_t conv2d_fprop_winograd(const igconv_problem_t* prob, igconv_dtype_t dtype,
+                                      const void* X, const void* Wt, const void* bias,
+                                      const void* Cin, void* Y, float alpha, float beta, int relu,
+                                      void* workspace, size_t workspace_bytes, void* stream) {
+  int P = 0, Q = 0;
+  igconv_status_t st = check_shape(prob, &P, &Q);
+  if (st != IGCONV_OK) return st;
+  if (!X || !Wt || !Y || (beta != 0.0f && !Cin)) return IGCONV_ERR_INVALID_ARG;
+  if (!std::isfinite(alpha) || !std::isfinite(beta)) return IGCONV_ERR_INVALID_ARG;
+  if (dtype != IGCONV_F16 && dtype != IGCONV_BF16) return IGCONV_ERR_UNSUPPORTED;
+  if (!wino_shape(prob)) return IGCONV_ERR_UNSUPPORTED;
+  if ((st = check_limits(prob, P, Q, 8)) != IGCONV_OK) return st;
+  WinoWs w;
+  if (!wino_ws(prob, P, Q, &w)) return IGCONV_ERR_UNSUPPORTED;
+  if (!aligned16(X) || !aligned16(Wt) || !aligned16(Y) || (bias && !aligned16(bias)) ||
+      (beta != 0.0f && !aligned16(Cin)) || (workspace && !aligned16(workspace)))
+    return IGCONV_ERR_MISALIGNED;
+  if (!workspace || workspace_bytes < w.total) return IGCONV_ERR_WORKSPACE;
+  DeviceState* dev = nullptr;
+  if ((st = device_state(&dev)) != IGCONV_OK) return st;
+  const int bf16 = dtype == IGCONV_BF16 ? 1 : 0;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint8_t* V = ws;
+  uint8_t* U = ws + w.v_bytes;
+  uint8_t* Mx = U + w.u_bytes;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  ConvGemmParams p;
+  init_common(p, dev);
+  const int tiles_m = ceil_div(w.T, kBlockM);
+  const int bn = choose_block_n(prob->K, 16LL * tiles_m, dev->sm_count);
+  p.tiles_n = ceil_div(prob->K, bn);
+  int tile_begin = 0;
+  for (int xi = 0; xi < 16; ++xi) {
+    SubProblem& sp = p.sub[xi];
+    sp.M = static_cast<int>(w.T);
+    sp.tile_begin = tile_begin;
+    sp.tiles_m = tiles_m;
+    sp.Hs = 1;
+    sp.Ws = static_cast<int>(w.T);
+    sp.lower_h = 0; sp.lower_w = 0; sp.trav_h = 1; sp.trav_w = 1;
+    sp.r0 = xi; sp.rstep = 1; sp.rcount = 1; sp.offh0 = 0; sp.doffh = 0;
+    sp.s0 = 0; sp.sstep = 1; sp.scount = 1; sp.offw0 = 0; sp.doffw = 0;
+    sp.out_h0 = xi; sp.out_w0 = 0; sp.out_sh = 1; sp.out_sw = 1;
+    if (!encode_im2col(&p.mapA[xi], V + static_cast<size_t>(xi) * w.T * prob->C * 2, bf16, 1, 1,
+                       static_cast<int>(w.T), prob->C, 0, 0, 0, 0, 1, 1, kBlockM))
+      return IGCONV_ERR_UNSUPPORTED;
+    p.mapA_valid |= 1u << xi;
+    tile_begin += tiles_m * p.tiles_n;
+  }
+  p.nsub = 16;
+  p.units = tile_begin;
+  p.a_src = SRC_IM2COL_K;
+  p.b_src = SRC_W_K;
+  p.cblocks = ceil_div(prob->C, kBlockK);
+  p.N_gemm = prob->K;
+  p.out_C = prob->K;
+  p.out_H = 16;
+  p.out_W = static_cast<int>(w.T);
+  p.idesc = make_idesc(kBlockM, bn, bf16, 0, 0);
+  set_fp_accumulators(p, bn);
+  if (!encode_filter(&p.mapB, U, bf16, prob->K, 16, 1, prob->C, bn)) return IGCONV_ERR_UNSUPPORTED;
+  p.epi = EPI_STORE;
+  p.out = Mx;
+  p.use_tma_store = 0;
+  p.alpha = 1.0f;
+  p.out_bf16 = bf16;
+  p.pf_base = U;
+  p.pf_bytes = static_cast<long long>(prob->K) * 16 * prob->C * 2;
+
+  cudaError_t e = launch_wino_input(X, V, prob->N, prob->H, prob->W, prob->C, w.TH, w.TW,
+                                    prob->pad_h, prob->pad_w, bf16, s);
+  if (e != cudaSuccess) return IGCONV_ERR_CUDA;
+  e = launch_wino_filter(Wt, U, prob->K, prob->C, bf16, s);
+  if (e != cudaSuccess) return IGCONV_ERR_CUDA;
+  e = launch_conv_gemm(p, bn, grid_for(p.units, dev), s);
+  if (e != cudaSuccess) return IGCONV_ERR_CUDA;
+  return from_cuda(launch_wino_output(Mx, Y, beta != 0.0f ? Cin : nullptr, bias, prob->N, P, Q,
+                                      prob->K, w.TH, w.TW, alpha, beta, relu ? 1 : 0, bf16, s));
 }
 
 igconv_status_t nchw_to_nhwc(const void* src, void* dst, int N, int C, int H, int W,

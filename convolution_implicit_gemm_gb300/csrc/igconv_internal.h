@@ -154,6 +154,12 @@ cudaError_t launch_group_filter64(const void* w, void* dst, int K, int RS, int c
                                   cudaStream_t s);
 cudaError_t launch_group_extract64(const float* src, void* dW, int dw_dtype, const void* cin,
                                    float beta, int K, int RS, int cg, cudaStream_t s);
+cudaError_t launch_wino_input(const void* X, void* V, int N, int H, int W, int C, int TH, int TW,
+                              int ph, int pw, int bf16, cudaStream_t s);
+cudaError_t launch_wino_filter(const void* Wt, void* U, int K, int C, int bf16, cudaStream_t s);
+cudaError_t launch_wino_output(const void* Mx, void* Y, const void* cin, const void* bias, int N,
+                               int P, int Q, int K, int TH, int TW, float alpha, float beta,
+                               int relu, int bf16, cudaStream_t s);
 cudaError_t launch_selftest_wait(unsigned int* status, unsigned long long timeout_ns,
                                  cudaStream_t s);
 cudaError_t status_word_address(unsigned int** ptr);

@@ -382,6 +382,35 @@ IGCONV_API igconv_status_t conv3d_wgrad(const igconv_problem3d_t *prob, igconv_d
                                         const void *Cin, void *dW, float alpha, float beta,
                                         void *workspace, size_t workspace_bytes, void *stream);
 
+/* Forward pass by Winograd's minimal filtering F(2x2, 3x3), for 3x3 filters
+ * at stride 1 and dilation 1 (tensorcore "docs/conv2d.md", "What's not done
+ * in v0.1", names it for 3x3 stride-1 layers with a 2-2.25x multiply
+ * saving).  Over 4x4 input patches d at stride 2 and each 3x3 filter g:
+ *   V = Bt d B,  U = G g Gt,  M[xi] = sum_c V[xi][c] U[xi][c],  Y = At M A
+ *   Bt = [1 0 -1 0; 0 1 1 0; 0 -1 1 0; 0 1 0 -1]
+ *   G  = [1 0 0; 1/2 1/2 1/2; 1/2 -1/2 1/2; 0 0 1],  At = [1 1 1 0; 0 1 -1 -1]
+ * which equals conv2d_fprop's sum in real arithmetic; then alpha, beta*Cin,
+ * bias, ReLU and the cast exactly as conv2d_fprop.  V, U and M are rounded to
+ * the 16-bit I/O type (round to nearest even); the 16 products sum over C in
+ * fp32 on the tensor cores (one implicit-GEMM launch, one sub-problem per
+ * transform point).  The result is therefore not bit-equal to conv2d_fprop;
+ * its error is bounded by the roundings of V, U and M (see the tests).
+ *   Arguments as conv2d_fprop, plus workspace (V [16][T][C], U [K][16][C],
+ *   M [16][T][K], T = N * ceil(P/2) * ceil(Q/2)) of at least
+ *   conv2d_fprop_winograd_workspace_size() bytes, caller-owned, overwritten,
+ *   not shared with a concurrent call.
+ *   R = S = 3, strides 1, dilations 1, C and K multiples of 8 (else
+ *   UNSUPPORTED; the size query returns 0).
+ * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, WORKSPACE, CUDA. */
+IGCONV_API size_t conv2d_fprop_winograd_workspace_size(const igconv_problem_t *prob,
+                                                       igconv_dtype_t dtype);
+IGCONV_API igconv_status_t conv2d_fprop_winograd(const igconv_problem_t *prob,
+                                                 igconv_dtype_t dtype, const void *X,
+                                                 const void *Wt, const void *bias,
+                                                 const void *Cin, void *Y, float alpha,
+                                                 float beta, int relu, void *workspace,
+                                                 size_t workspace_bytes, void *stream);
+
 /* Bytes of device workspace conv2d_fprop_int8 needs (fp16 copies of X and
  * Wt, which the tensor cores consume).  Host only; 0 for an invalid problem. */
 IGCONV_API size_t conv2d_fprop_int8_workspace_size(const igconv_problem_t *prob);
