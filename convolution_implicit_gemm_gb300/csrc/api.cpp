@@ -45,7 +45,8 @@ std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 PFN_encodeTiled g_encode_tiled = nullptr;
 PFN_encodeIm2col g_encode_im2col = nullptr;
-std::atomic<int> g_tune_splits{0}, g_tune_bn{0}, g_tune_max_ctas{0}, g_tune_no_pairs{0};
+std::atomic<int> g_tune_splits{0}, g_tune_bn{0}, g_tune_max_ctas{0}, g_tune_no_pairs{0},
+    g_tune_epi_groups{0};
 
 igconv_status_t device_state(DeviceState** out) {
   int dev = 0;
@@ -311,6 +312,7 @@ void init_common(ConvGemmParams& p, const DeviceState* st) {
   p.num_acc = 1;
   p.kb_per_acc = 1 << 30;
   p.splits = 1;
+  p.epi_groups = g_tune_epi_groups.load();  // 0: the launcher decides
 }
 
 // fprop plan (16-bit, or the int8 path's widened copies) on X [N,H,W,C],
@@ -964,6 +966,10 @@ igconv_status_t igconv_set_tuning(igconv_tune_key_t key, int value) {
     case IGCONV_TUNE_CTA_PAIRS:
       if (value < 0 || value > 2) return IGCONV_ERR_INVALID_ARG;
       g_tune_no_pairs.store(value);
+      return IGCONV_OK;
+    case IGCONV_TUNE_EPI_GROUPS:
+      if (value < 0 || value > 2) return IGCONV_ERR_INVALID_ARG;
+      g_tune_epi_groups.store(value);
       return IGCONV_OK;
   }
   return IGCONV_ERR_INVALID_ARG;

@@ -62,7 +62,7 @@ struct Cfg {
   static constexpr int STAGES = PAIR ? (BN == 256 ? 6 : 8) : (BN == 256 ? 4 : (BN == 128 ? 6 : 8));
   static constexpr int PIPE = STAGE * STAGES;
   static constexpr int EPI_STAGE = kEpiWarps * kStageWarpBytes;  // 32 KB
-  static constexpr int BAR_BYTES = 192;
+  static constexpr int BAR_BYTES = 256;
   static constexpr int NI = (BN == 256) ? 1 : 2;  // MMA issuer threads
   // Producer warps: one thread needs ~600 cycles per stage (barrier wait,
   // expect-tx and copy issue each take 100-250 cycles), so one lane in each
@@ -75,7 +75,8 @@ struct Cfg {
   static constexpr int USED = PIPE + EPI_STAGE + kBiasBytes + BAR_BYTES;
   static constexpr int SMEM = kSmemLimit;
   static_assert(USED <= kSmemLimit, "exceeds the 227 KB of shared memory a CTA may use");
-  static_assert(2 * STAGES + 6 <= (BAR_BYTES - 8) / 8, "barrier area too small");
+  // full/empty per stage, tfull/tempty per TMEM buffer (up to 4), done per issuer
+  static_assert(2 * STAGES + 10 <= (BAR_BYTES - 8) / 8, "barrier area too small");
 };
 
 struct Work {
@@ -591,14 +592,17 @@ __device__ __forceinline__ void run_mma(const ConvGemmParams& p, uint8_t* pipe, 
   int stage = 0;        // stage of the first block of the next unit
   uint32_t phase = 0;
   int local = 0;
+  // TMEM buffers: two, or four when two epilogue groups take alternate tiles
+  const int buf_shift = p.epi_groups == 2 ? 2 : 1;
+  const int buf_mask = (1 << buf_shift) - 1;
   bool ok = true;
   UnitWalk uw;
   for (walk_begin(p, sc, uw); ok && uw.u < sc.units; walk_next(sc, uw)) {
     const Work w = walk_work(p, sc, uw);
     const int nk = w.kb1 - w.kb0;
     if (nk <= 0) continue;  // no reduction: the epilogue writes beta*Cin alone
-    const int buf = local & 1;
-    const uint32_t tph = static_cast<uint32_t>(local >> 1) & 1u;
+    const int buf = local & buf_mask;
+    const uint32_t tph = static_cast<uint32_t>(local >> buf_shift) & 1u;
     if (!__all_sync(0xffffffffu, mbar_wait(&tempty[buf], tph ^ 1u, abort_flag, timeout))) {
       if (lane == 0) report_failure(p, abort_flag, DEVERR_MMA_TMEM_WAIT);
       break;
@@ -937,14 +941,24 @@ __device__ __forceinline__ void run_epilogue(const ConvGemmParams& p, uint64_t* 
   const long long rq_half_m1 = rq_plain ? (1LL << (rq_sh - 1)) - 1 : 0;
 
   const int quarter = warp & 3;
-  const int half = (warp - kEpiWarp0) >> 2;   // which half of the tile's columns
+  // One group: warps 4-7 take the first half of every tile's columns and
+  // warps 8-11 the second.  Two groups: warps 4-7 take the tiles with even
+  // accumulator sequence number whole and warps 8-11 the odd ones, each
+  // group double-buffered in its own two of four TMEM buffers, so every
+  // buffer is only ever waited on by one group, in order.
+  const int groups = p.epi_groups == 2 ? 2 : 1;
+  const int group = groups == 2 ? (warp - kEpiWarp0) >> 2 : 0;
+  const int half = groups == 2 ? 0 : (warp - kEpiWarp0) >> 2;   // which half of the columns
+  const int buf_shift = groups == 2 ? 2 : 1;
+  const int buf_mask = (1 << buf_shift) - 1;
   const int lane = threadIdx.x & 31;
   const int row = quarter * 32 + lane;
   uint8_t* stage = stage_buf + (warp - kEpiWarp0) * kStageWarpBytes;
   const int j0 = half * (BN / 64);
-  const int j1 = j0 + BN / 64;
+  const int j1 = groups == 2 ? BN / 32 : j0 + BN / 64;
   int flip = 0;  // staging buffer to use next
   int local = 0;
+  int plain = 0;  // units without accumulators seen so far (they alternate between groups)
   int qseq = 0;  // sequence number of the next reduction block (see run_mma)
   const int M0 = p.sub[0].M;  // GEMM rows when there is one sub-problem
   const bool one_sub = e.sc.nsub == 1;
@@ -958,8 +972,12 @@ __device__ __forceinline__ void run_epilogue(const ConvGemmParams& p, uint64_t* 
     // which of the first NI accumulators hold blocks (NI == 2: at least one)
     const bool use1 = NI >= 2 && acc_used(e.kb_per_acc, 1, NI, nk, q0);
     const uint32_t lone = (NI >= 2 && !acc_used(e.kb_per_acc, 0, NI, nk, q0)) ? BN : 0u;
-    const int buf = local & 1;
-    const uint32_t tph = static_cast<uint32_t>(local >> 1) & 1u;
+    const int buf = local & buf_mask;
+    const uint32_t tph = static_cast<uint32_t>(local >> buf_shift) & 1u;
+    if (groups == 2 && ((has_acc ? local : plain) & 1) != group) {
+      if (has_acc) ++local; else ++plain;  // the other group's unit
+      continue;
+    }
     if (has_acc) {
       if (!mbar_wait(&tfull[buf], tph, abort_flag, e.timeout)) {
         report_failure(p, abort_flag, DEVERR_EPI_WAIT);
@@ -1293,6 +1311,8 @@ __device__ __forceinline__ void run_epilogue(const ConvGemmParams& p, uint64_t* 
           mbar_arrive(&tempty[buf]);
       }
       ++local;
+    } else {
+      ++plain;
     }
   }
   // every TMA store this warp issued must complete before the CTA exits
@@ -1330,14 +1350,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::PIPE + C::EPI_STAGE + kBiasBytes);
   uint64_t* empty = full + C::STAGES;
   uint64_t* tfull = empty + C::STAGES;
-  uint64_t* tempty = tfull + 2;
-  uint64_t* done_bar = tempty + 2;  // one per issuer
+  uint64_t* tempty = tfull + 4;
+  uint64_t* done_bar = tempty + 4;  // one per issuer
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t tmem_cols = tmem_cols_for(static_cast<uint32_t>(2 * p.num_acc * BN));
+  const int nbuf = p.epi_groups == 2 ? 4 : 2;  // TMEM accumulator buffers
+  const uint32_t tmem_cols = tmem_cols_for(static_cast<uint32_t>(nbuf * p.num_acc * BN));
   const int rank = PAIR ? static_cast<int>(cluster_ctarank() & 1u) : 0;
 
   if (threadIdx.x == 0) {
@@ -1345,11 +1366,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(&tfull[0], C::NI);
-    mbar_init(&tfull[1], C::NI);
-    // with pairs the even CTA's TMEM-empty barriers count both CTAs' epilogues
-    mbar_init(&tempty[0], PAIR ? 2 * kEpiWarps : kEpiWarps);
-    mbar_init(&tempty[1], PAIR ? 2 * kEpiWarps : kEpiWarps);
+    // a tile's epilogue is 8 warps (one group) or 4 (two groups); with pairs
+    // the even CTA's TMEM-empty barriers count both CTAs' epilogues
+    const int epi_warps = p.epi_groups == 2 ? kEpiWarps / 2 : kEpiWarps;
+    for (int b = 0; b < 4; ++b) {
+      mbar_init(&tfull[b], C::NI);
+      mbar_init(&tempty[b], PAIR ? 2 * epi_warps : epi_warps);
+    }
     mbar_init(&done_bar[0], 1);
     mbar_init(&done_bar[1], 1);
     *abort_flag = 0;
@@ -1503,7 +1526,20 @@ size_t conv_gemm_smem_bytes(int block_n) {
   }
 }
 
-cudaError_t launch_conv_gemm(const ConvGemmParams& p, int block_n, int grid, cudaStream_t s) {
+cudaError_t launch_conv_gemm(const ConvGemmParams& p_in, int block_n, int grid, cudaStream_t s) {
+  // Two epilogue groups with four TMEM buffers pay where the epilogue, not
+  // the main loop, sets the pace: 64-wide tiles (whose four buffers of two
+  // issuers' accumulators fill the 512 TMEM columns) with at most four
+  // reduction blocks per unit.  epi_groups: 0 decide here, 1 never, 2
+  // whenever the buffers fit.
+  ConvGemmParams p = p_in;
+  const bool fits = block_n == 64 && !p.pair && p.epi != EPI_PARTIAL && 4 * p.num_acc * 64 <= 512;
+  int max_kb = 0;
+  for (int i = 0; i < p.nsub; ++i) {
+    const int kb = p.sub[i].rcount * p.sub[i].scount * p.cblocks;
+    if (kb > max_kb) max_kb = kb;
+  }
+  p.epi_groups = (fits && (p.epi_groups == 2 || (p.epi_groups == 0 && max_kb <= 4))) ? 2 : 1;
   switch (block_n) {
     case 64: return p.pair ? launch_bn<64, true>(p, grid, s) : launch_bn<64, false>(p, grid, s);
     case 128: return p.pair ? launch_bn<128, true>(p, grid, s) : launch_bn<128, false>(p, grid, s);

@@ -512,12 +512,19 @@ IGCONV_API const char *igconv_status_string(igconv_status_t status);
  *                             SMs sharing 256-row MMAs); 1: never; 2: with
  *                             256-wide tiles as well.
  *                             Results are bit-identical either way.
+ *   IGCONV_TUNE_EPI_GROUPS    0: 64-wide tiles with at most four reduction
+ *                             blocks per tile (unpaired, not the wgrad
+ *                             partials) run their epilogue as two groups of
+ *                             four warps taking alternate tiles, with four
+ *                             TMEM buffers; 1: never; 2: whenever the four
+ *                             buffers fit.  Results are bit-identical.
  * Returns INVALID_ARG for an unknown key or value. */
 typedef enum {
     IGCONV_TUNE_WGRAD_SPLITS = 1,
     IGCONV_TUNE_BLOCK_N = 2,
     IGCONV_TUNE_MAX_CTAS = 3,
-    IGCONV_TUNE_CTA_PAIRS = 4
+    IGCONV_TUNE_CTA_PAIRS = 4,
+    IGCONV_TUNE_EPI_GROUPS = 5
 } igconv_tune_key_t;
 IGCONV_API igconv_status_t igconv_set_tuning(igconv_tune_key_t key, int value);
 

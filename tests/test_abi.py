@@ -155,6 +155,10 @@ def test_tuning_keys(igc):
     assert lib.igconv_set_tuning(igc.TUNE_WGRAD_SPLITS, -1) == 1
     assert lib.igconv_set_tuning(igc.TUNE_BLOCK_N, 128) == 0
     assert lib.igconv_set_tuning(igc.TUNE_BLOCK_N, 0) == 0
+    assert lib.igconv_set_tuning(igc.TUNE_EPI_GROUPS, 3) == 1
+    assert lib.igconv_set_tuning(igc.TUNE_EPI_GROUPS, -1) == 1
+    assert lib.igconv_set_tuning(igc.TUNE_EPI_GROUPS, 2) == 0
+    assert lib.igconv_set_tuning(igc.TUNE_EPI_GROUPS, 0) == 0
     assert lib.igconv_set_tuning(igc.TUNE_CTA_PAIRS, 3) == 1
     assert lib.igconv_set_tuning(igc.TUNE_CTA_PAIRS, 2) == 0
     assert lib.igconv_set_tuning(igc.TUNE_CTA_PAIRS, 1) == 0
