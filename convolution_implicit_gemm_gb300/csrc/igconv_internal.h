@@ -122,9 +122,9 @@ struct ConvGemmParams {
   int ws_ld;                  // wgrad: padded N extent
   uint32_t rq_mant;           // int8: multiplier M = rq_mant * 2^rq_exp exactly
   int rq_exp;
-  int epi_groups;             // epilogue warp groups: 0 the launcher decides, 1 one group of
-                              // eight warps per tile (two TMEM buffers), 2 two groups of four
-                              // taking alternate tiles whole (four buffers) where they fit
+  int epi_groups;             // epilogue warp groups: 0 or 2 two groups of four taking
+                              // alternate tiles whole (four TMEM buffers) where they fit,
+                              // 1 one group of eight warps per tile (two buffers)
   int int_acc;                // 1: the accumulators hold exact integers (int8 operands on the
                               // fp16 path); EPI_STORE writes their int32 sum, EPI_PARTIAL
                               // int32 partial sums (int8 dgrad / wgrad)

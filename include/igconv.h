@@ -512,12 +512,12 @@ IGCONV_API const char *igconv_status_string(igconv_status_t status);
  *                             SMs sharing 256-row MMAs); 1: never; 2: with
  *                             256-wide tiles as well.
  *                             Results are bit-identical either way.
- *   IGCONV_TUNE_EPI_GROUPS    0: 64-wide tiles with at most four reduction
- *                             blocks per tile (unpaired, not the wgrad
- *                             partials) run their epilogue as two groups of
- *                             four warps taking alternate tiles, with four
- *                             TMEM buffers; 1: never; 2: whenever the four
- *                             buffers fit.  Results are bit-identical.
+ *   IGCONV_TUNE_EPI_GROUPS    0 or 2: 64-wide tiles (unpaired, not the
+ *                             wgrad partials) run their epilogue as two
+ *                             groups of four warps taking alternate tiles,
+ *                             with four TMEM buffers; 1: one group of eight
+ *                             warps per tile, two buffers.  Results are
+ *                             bit-identical.
  * Returns INVALID_ARG for an unknown key or value. */
 typedef enum {
     IGCONV_TUNE_WGRAD_SPLITS = 1,

@@ -1,6 +1,6 @@
 """The two-group epilogue (two groups of four warps taking alternate tiles
 whole, four TMEM buffers) against the one-group epilogue, on the layers it
-is chosen for: 64-wide tiles with at most four reduction blocks per tile.
+is chosen for: 64-wide tiles, short and long reductions.
 Every output must be bit-identical either way (each row gets the same
 accumulators and the same epilogue arithmetic) and, on integer data, equal
 to the oracle.  The cases include strided dgrad with residue classes that
@@ -54,6 +54,7 @@ DGRAD = [
     problem(2, 17, 19, 64, 48, 3, 3, (0, 0), (4, 4)),      # stride 4: classes with no taps
     problem(3, 15, 13, 64, 256, 1, 1),                     # 1x1: four blocks per tile
     problem(1, 9, 11, 48, 64, 1, 1, (0, 0), (2, 2)),       # 1x1 strided: uncovered rows
+    problem(2, 20, 18, 64, 128, 3, 3, (1, 1)),             # stride 1, 18 blocks per tile
 ]
 
 
