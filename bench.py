@@ -353,17 +353,69 @@ def volume_pass(name, kind, device="cuda"):
                                     need)
 
 
+def int8_pass(kind, device="cuda"):
+    """One pass of the int8 workload (64 x 56 x 56, 128 -> 128, 3x3) as a
+    callable: the requantised forward pass, or the int32 data / weight
+    gradient."""
+    import convolution_implicit_gemm_gb300 as igc
+    wl = WORKLOADS["int8_56x56_128to128_3x3"]
+    pb = wl["problem"]
+    P, Q = igc.conv2d_output_size(pb)
+    inp = make_inputs(pb, P, Q, "i8", "int8", wl["seed"], bias=True)
+    X, Wt, b, dY = (inp[k].to(device) for k in ("X", "W", "bias", "dY"))
+    if kind == "fprop":
+        Y = torch.empty((pb["N"], P, Q, pb["K"]), dtype=torch.int8, device=device)
+        need = igc.conv2d_fprop_int8_workspace_size(pb)
+        ws = torch.empty(need, dtype=torch.uint8, device=device)
+        return lambda: igc.conv2d_fprop_int8(pb, X, Wt, b, Y, wl["act_scale"], wl["w_scale"],
+                                             wl["out_scale"], True, ws, need)
+    if kind == "dgrad":
+        dX = torch.empty((pb["N"], pb["H"], pb["W"], pb["C"]), dtype=torch.int32, device=device)
+        ws = torch.empty(igc.conv2d_dgrad_int8_workspace_size(pb), dtype=torch.uint8,
+                         device=device)
+        return lambda: igc.conv2d_dgrad_int8(pb, dY, Wt, dX, ws)
+    dW = torch.empty((pb["K"], pb["R"], pb["S"], pb["C"]), dtype=torch.int32, device=device)
+    ws = torch.empty(igc.conv2d_wgrad_int8_workspace_size(pb), dtype=torch.uint8, device=device)
+    return lambda: igc.conv2d_wgrad_int8(pb, X, dY, dW, ws)
+
+
+def permute_pass(kind, device="cuda"):
+    """The permute of the first sweep layer's activations (128 x 64 x 56 x
+    56 bf16), NCHW -> NHWC or back."""
+    import convolution_implicit_gemm_gb300 as igc
+    pb = WORKLOADS[RESNET50_SWEEP[0]]["problem"]
+    N, C, H, W = pb["N"], pb["C"], pb["H"], pb["W"]
+    src = torch.randn((N, C, H, W), device=device).to(torch.bfloat16)
+    dst = torch.empty((N, H, W, C), dtype=torch.bfloat16, device=device)
+    if kind == "nchw_to_nhwc":
+        return lambda: igc.nchw_to_nhwc(src, dst, N, C, H, W)
+    return lambda: igc.nhwc_to_nchw(dst, src, N, C, H, W)
+
+
 def run_only(args):
     """One pass of one workload, launched warmup + steps times on cuda:0 (for
-    ncu captures: skip `warmup` launches of the kernel, capture the next)."""
+    ncu captures: skip `warmup` launches of the kernel, capture the next).
+    LAYER:PASS takes the sweep and row workloads (PASS fprop, dgrad, wgrad,
+    or winograd for a 3x3 stride-1 layer), int8_56x56_128to128_3x3:PASS the
+    int8 passes, permute:nchw_to_nhwc / permute:nhwc_to_nchw the permutes."""
     import convolution_implicit_gemm_gb300 as igc
     igc.load()
     name, kind = args.only.split(":")
-    if "problem3d" in WORKLOADS[name]:
+    if name == "permute":
+        fn = permute_pass(kind)
+    elif name == "int8_56x56_128to128_3x3":
+        fn = int8_pass(kind)
+    elif "problem3d" in WORKLOADS[name]:
         fn = volume_pass(name, kind)
     else:
         L = Layer(name, batch=args.batch)
-        fn = getattr(L, kind)
+        if kind == "winograd":
+            need = igc.conv2d_fprop_winograd_workspace_size(L.pb, L.td)
+            ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+            fn = lambda: igc.conv2d_fprop_winograd(L.pb, L.td, L.X, L.W, L.b, None, L.Y,  # noqa
+                                                   1.0, 0.0, L.relu, ws)
+        else:
+            fn = getattr(L, kind)
     for _ in range(args.warmup):
         fn()
     torch.cuda.synchronize()
