@@ -548,7 +548,8 @@ struct WgradPlan {
 // rows), the tile width and the split count are chosen together, minimising
 // (waves of persistent CTAs) x (columns x reduction blocks per unit) / (tile
 // efficiency).  Splits fill at most one wave and keep >= 8 blocks each.
-void plan_wgrad_shape(const igconv_problem_t* pb, int P, int Q, int sm_count, WgradPlan* w) {
+void plan_wgrad_shape(const igconv_problem_t* pb, int P, int Q, int sm_count, WgradPlan* w,
+                      int max_bn = 256) {
   const int sms = sm_count > 0 ? sm_count : 148;
   w->rs = pb->R * pb->S;
   w->cblocks = ceil_div(pb->C, kBlockK);
@@ -565,6 +566,7 @@ void plan_wgrad_shape(const igconv_problem_t* pb, int P, int Q, int sm_count, Wg
     const int cands[3] = {256, 128, 64};
     for (int bn : cands) {
       if (forced_bn && bn != forced_bn) continue;
+      if (!forced_bn && bn > max_bn) continue;
       const int tiles_m = ceil_div(mext, kBlockM);
       const int tiles_n = ceil_div(next, bn);
       const long long tiles = static_cast<long long>(tiles_m) * tiles_n;
@@ -891,7 +893,10 @@ bool int_accumulators(int bn, int max_kb, int* num_acc, int* kb_per_acc) {
 // wgrad plan of the int8 path: the fp16 plan, with the split count raised
 // until every split's reduction fits the accumulators of its tile width.
 void plan_wgrad_int8(const igconv_problem_t* pb, int P, int Q, int sm_count, WgradPlan* w) {
-  plan_wgrad_shape(pb, P, Q, sm_count, w);
+  // a 256-wide tile has one issuer and room for one accumulator per TMEM
+  // buffer (16 blocks per split); 128- and 64-wide tiles have two issuers
+  // and room for 32 and 64 blocks, so far fewer splits and partials
+  plan_wgrad_shape(pb, P, Q, sm_count, w, 128);
   const int ni = issuers_for(w->bn);
   const int max_groups = 512 / (2 * ni * w->bn);
   const int max_kb = ni * (max_groups < 1 ? 1 : max_groups) * 16;

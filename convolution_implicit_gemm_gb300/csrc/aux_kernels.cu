@@ -514,9 +514,9 @@ cudaError_t launch_wgrad_reduce(const float* ws, int splits, long long split_str
 }
 
 // ---------------------------------------------------------------------------
-// int8 wgrad: dW[k][rs][c] (int32) = the int32 partial tiles of the splits
-// added in split order, wrapping modulo 2^32 like the int32 accumulator they
-// stand for.  One thread per element of the partial matrix, so the reads of
+// int8 wgrad: dW[k][rs][c] (int32) = the sum of the int32 partial tiles of
+// the splits, wrapping modulo 2^32 like the int32 accumulator they stand for
+// (exact and order-independent).  One thread per element of the partial matrix, so the reads of
 // every split run along its rows; rows past the valid extent are skipped.
 //   not swapped: rows (tap, c) over rs * cpad, columns k
 //   swapped:     rows k, columns (tap, c)
@@ -535,9 +535,20 @@ __global__ void __launch_bounds__(256) wgrad_reduce_i32_kernel(
     const int c = x - rs * cpad;
     if (k >= K || rs >= RS || c >= C) continue;
     const int* src = ws + static_cast<long long>(m) * ws_ld + n;
+    // eight independent loads in flight; integer addition modulo 2^32 is
+    // associative, so the grouping changes no bit of the result
+    uint32_t acc[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    int sp = 0;
+    for (; sp + 8 <= splits; sp += 8) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        acc[i] += static_cast<uint32_t>(__ldcs(src + static_cast<long long>(sp + i) * split_stride));
+    }
+    for (; sp < splits; ++sp)
+      acc[0] += static_cast<uint32_t>(__ldcs(src + static_cast<long long>(sp) * split_stride));
     uint32_t sum = 0u;
-    for (int sp = 0; sp < splits; ++sp)
-      sum += static_cast<uint32_t>(src[static_cast<long long>(sp) * split_stride]);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sum += acc[i];
     dW[(static_cast<long long>(k) * RS + rs) * C + c] = static_cast<int>(sum);
   }
 }

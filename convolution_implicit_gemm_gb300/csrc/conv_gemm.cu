@@ -692,35 +692,21 @@ __device__ __forceinline__ void unpack8(uint4 v, float (&f)[8], int bf16) {
   }
 }
 
-// round_half_even(t * M) clamped to int8, with M = mant * 2^exp exactly.
-// |t| < 2^33 and mant < 2^24, so t * mant fits in int64.
-__device__ __forceinline__ int requant_exact(long long t, uint32_t mant, int exp) {
-  const long long prod = t * static_cast<long long>(mant);
-  if (exp >= 0) {
-    if (prod == 0) return 0;
-    return prod > 0 ? 127 : -128;  // |prod| >= 2^23 whenever t != 0
-  }
-  const int sh = -exp;
-  if (sh >= 62) return 0;  // |t * M| < 2^57 / 2^62 < 0.5
-  long long q = prod >> sh;  // floor
-  const long long rem = prod - (q << sh);
-  const long long half = 1LL << (sh - 1);
-  if (rem > half || (rem == half && (q & 1LL))) q += 1;
-  if (q > 127) q = 127;
-  if (q < -128) q = -128;
-  return static_cast<int>(q);
-}
-
 // round_half_even(t * M) clamped to int8 without branches, for M = mant *
-// 2^-sh with 1 <= sh <= 62 and |t| < 2^33: with x = t * mant (exact in 64
+// 2^-sh and |t| < 2^33.  For 1 <= sh <= 62: with x = t * mant (exact in 64
 // bits) and b the lowest bit of floor(x / 2^sh), the quotient
 // floor((x + b + 2^(sh-1) - 1) / 2^sh) rounds x / 2^sh to nearest with ties to
 // the even neighbour (an arithmetic shift is the floor, also for negative x).
+// sh <= 0 means M >= 2^23, so every t != 0 saturates; sh >= 63 means M <
+// 2^-39, so |t * M| < 1/2 rounds to 0.  The caller passes sh clamped to
+// 1..62 and the mode of the true shift (0 in range, 1 saturate, 2 zero).
 __device__ __forceinline__ int requant_rne(long long t, uint32_t mant, int sh,
-                                          long long half_m1) {
+                                          long long half_m1, int mode) {
   const long long x = t * static_cast<long long>(mant);
   const long long b = (x >> sh) & 1LL;
   long long q = (x + b + half_m1) >> sh;
+  if (mode == 1) q = t > 0 ? 127 : (t < 0 ? -128 : 0);
+  if (mode == 2) q = 0;
   q = q > 127 ? 127 : q;
   q = q < -128 ? -128 : q;
   return static_cast<int>(q);
@@ -934,11 +920,11 @@ __device__ __forceinline__ void run_epilogue(const ConvGemmParams& p, uint64_t* 
   // the 16-bit passes, int32 for int8); every lane reads the same entries,
   // so the reads are shared-memory broadcasts.
   const bool bias_cached = p.bias_cached != 0;
-  // int8 multiplier M = rq_mant * 2^-rq_sh; shifts of 1..62 take the
-  // branch-free rounding (every M of practical size: 2^-38 < M < 2^23)
-  const int rq_sh = -e.rq_exp;
-  const bool rq_plain = rq_sh >= 1 && rq_sh <= 62;
-  const long long rq_half_m1 = rq_plain ? (1LL << (rq_sh - 1)) - 1 : 0;
+  // int8 multiplier M = rq_mant * 2^-rq_sh (uniform across the launch)
+  const int rq_sh_true = -e.rq_exp;
+  const int rq_mode = rq_sh_true < 1 ? 1 : (rq_sh_true > 62 ? 2 : 0);
+  const int rq_sh = rq_sh_true < 1 ? 1 : (rq_sh_true > 62 ? 62 : rq_sh_true);
+  const long long rq_half_m1 = (1LL << (rq_sh - 1)) - 1;
 
   const int quarter = warp & 3;
   // One group: warps 4-7 take the first half of every tile's columns and
@@ -1157,8 +1143,7 @@ __device__ __forceinline__ void run_epilogue(const ConvGemmParams& p, uint64_t* 
             // |acc| <= 4096 * 2^14 = 2^26, so |t| < 2^32: exact in 64 bits
             long long t = static_cast<long long>(iacc[i]) + bv[i];
             if (e.relu && t < 0) t = 0;
-            const int y = rq_plain ? requant_rne(t, e.rq_mant, rq_sh, rq_half_m1)
-                                   : requant_exact(t, e.rq_mant, e.rq_exp);
+            const int y = requant_rne(t, e.rq_mant, rq_sh, rq_half_m1, rq_mode);
             packed[i >> 2] |= (static_cast<uint32_t>(y) & 0xFFu) << (8 * (i & 3));
           }
           const uint4 o[2] = {make_uint4(packed[0], packed[1], packed[2], packed[3]),
