@@ -191,10 +191,15 @@ class Layer:
         self.ws_bytes = igc.conv2d_grouped_wgrad_workspace_size(pb, self.groups, self.td,
                                                                 self.tdw)
         self.ws = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device=device)
-        # few input channels: fprop's pixel and filter copies
+        # few input channels: fprop's pixel and filter copies; more channels:
+        # the split-K partials, when the plan splits
         self.fws_bytes = igc.conv2d_fprop_workspace_size(pb, self.td)
         self.fws = (torch.empty(self.fws_bytes, dtype=torch.uint8, device=device)
                     if self.fws_bytes else None)
+        # unit-stride dgrad: the split-K workspace, when the plan splits
+        self.dws_bytes = (igc.conv2d_dgrad_workspace_size(pb, self.td) if self.groups == 1 else 0)
+        self.dws = (torch.empty(self.dws_bytes, dtype=torch.uint8, device=device)
+                    if self.dws_bytes else None)
         self.flops = conv_flops(pb, self.P, self.Q) / self.groups
         # grouped: the workspace that opens the tensor-core fprop / dgrad path
         self.gws_bytes = (igc.conv2d_grouped_fprop_workspace_size(pb, self.groups, self.td)
@@ -216,6 +221,9 @@ class Layer:
         if self.groups > 1:
             self.igc.conv2d_grouped_dgrad_ws(self.pb, self.groups, self.td, self.dY, self.W, None,
                                              self.dX, 1.0, 0.0, self.gws)
+        elif self.dws is not None:
+            self.igc.conv2d_dgrad_ws(self.pb, self.td, self.dY, self.W, None, self.dX, 1.0, 0.0,
+                                     self.dws)
         else:
             self.igc.conv2d_dgrad(self.pb, self.td, self.dY, self.W, None, self.dX, 1.0, 0.0)
 

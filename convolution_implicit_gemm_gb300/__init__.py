@@ -22,7 +22,7 @@ import torch
 __all__ = [
     "IgconvError", "Problem", "library_path", "load",
     "conv2d_output_size", "conv2d_fprop", "conv2d_fprop_workspace_size", "conv2d_fprop_ws",
-    "conv2d_dgrad", "conv2d_wgrad_workspace_size",
+    "conv2d_dgrad", "conv2d_dgrad_workspace_size", "conv2d_dgrad_ws", "conv2d_wgrad_workspace_size",
     "conv2d_wgrad", "conv2d_fprop_int8_workspace_size", "conv2d_fprop_int8",
     "conv2d_dgrad_int8_workspace_size", "conv2d_dgrad_int8", "conv2d_wgrad_int8_workspace_size",
     "conv2d_wgrad_int8", "conv2d_fprop_winograd_workspace_size", "conv2d_fprop_winograd",
@@ -37,6 +37,7 @@ __all__ = [
     "fprop", "dgrad", "wgrad", "fprop_int8",
     "F16", "BF16", "F32", "I8", "I32",
     "TUNE_WGRAD_SPLITS", "TUNE_BLOCK_N", "TUNE_MAX_CTAS", "TUNE_CTA_PAIRS", "TUNE_EPI_GROUPS",
+    "TUNE_CONV_SPLITS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -44,6 +45,7 @@ _LIB_PATH = os.path.join(_HERE, "libigconv.so")
 
 F16, BF16, F32, I8, I32 = 0, 1, 2, 3, 4
 TUNE_WGRAD_SPLITS, TUNE_BLOCK_N, TUNE_MAX_CTAS, TUNE_CTA_PAIRS, TUNE_EPI_GROUPS = 1, 2, 3, 4, 5
+TUNE_CONV_SPLITS = 6
 STATUS_NAMES = {0: "IGCONV_OK", 1: "IGCONV_ERR_INVALID_ARG", 2: "IGCONV_ERR_UNSUPPORTED",
                 3: "IGCONV_ERR_MISALIGNED", 4: "IGCONV_ERR_WORKSPACE", 5: "IGCONV_ERR_CUDA",
                 6: "IGCONV_ERR_DEVICE_TIMEOUT"}
@@ -113,6 +115,8 @@ def load():
             "conv2d_fprop_workspace_size": (SZ, [PP, I]),
             "conv2d_fprop_ws": (I, [PP, I, P, P, P, P, P, F, F, I, P, SZ, P]),
             "conv2d_dgrad": (I, [PP, I, P, P, P, P, F, F, P]),
+            "conv2d_dgrad_workspace_size": (SZ, [PP, I]),
+            "conv2d_dgrad_ws": (I, [PP, I, P, P, P, P, F, F, P, SZ, P]),
             "conv2d_wgrad_workspace_size": (SZ, [PP, I, I]),
             "conv2d_wgrad": (I, [PP, I, I, P, P, P, P, F, F, P, SZ, P]),
             "conv2d_fprop_int8_workspace_size": (SZ, [PP]),
@@ -253,6 +257,29 @@ def conv2d_dgrad(prob, dtype, dY, Wt, Cin, dX, alpha=1.0, beta=0.0, stream=None)
                                _ptr(Cin) if beta != 0.0 else None, _ptr(dX), float(alpha),
                                float(beta), _stream(stream)),
            "conv2d_dgrad")
+
+
+def conv2d_dgrad_workspace_size(prob, dtype) -> int:
+    pb = Problem.make(prob)
+    return int(load().conv2d_dgrad_workspace_size(ctypes.byref(pb), _dtype_code(dtype)))
+
+
+def conv2d_dgrad_ws(prob, dtype, dY, Wt, Cin, dX, alpha=1.0, beta=0.0, workspace=None,
+                    workspace_bytes=None, stream=None):
+    pb = Problem.make(prob)
+    P, Q = conv2d_output_size(pb)
+    _expect(dY, pb.N * P * Q * pb.K, "dY")
+    _expect(Wt, pb.K * pb.R * pb.S * pb.C, "Wt")
+    _expect(dX, pb.N * pb.H * pb.W * pb.C, "dX")
+    if beta != 0.0:
+        _expect(Cin, pb.N * pb.H * pb.W * pb.C, "Cin")
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().conv2d_dgrad_ws(ctypes.byref(pb), _dtype_code(dtype), _ptr(dY), _ptr(Wt),
+                                  _ptr(Cin) if beta != 0.0 else None, _ptr(dX), float(alpha),
+                                  float(beta), _ptr(workspace), int(workspace_bytes),
+                                  _stream(stream)),
+           "conv2d_dgrad_ws")
 
 
 def conv2d_wgrad_workspace_size(prob, dtype, dw_dtype) -> int:

@@ -46,7 +46,7 @@ DeviceState g_dev[kMaxDevices];
 PFN_encodeTiled g_encode_tiled = nullptr;
 PFN_encodeIm2col g_encode_im2col = nullptr;
 std::atomic<int> g_tune_splits{0}, g_tune_bn{0}, g_tune_max_ctas{0}, g_tune_no_pairs{0},
-    g_tune_epi_groups{0};
+    g_tune_epi_groups{0}, g_tune_conv_splits{0};
 
 igconv_status_t device_state(DeviceState** out) {
   int dev = 0;
@@ -906,6 +906,60 @@ void plan_wgrad_int8(const igconv_problem_t* pb, int P, int Q, int sm_count, Wgr
   w->ws_bytes = static_cast<size_t>(w->splits) * w->M_pad * w->N_pad * sizeof(int32_t);
 }
 
+// Split-K for the forward and stride-1 data passes (single sub-problem,
+// single CTAs): when whole tiles leave the last wave of persistent CTAs
+// mostly empty, each tile's reduction is cut into `splits` equal ranges and
+// the fp32 partial tiles are added in order by a reduction that also applies
+// the epilogue.  Model: waves x blocks per unit; a split must save at least
+// a fifth of that and keep 8 blocks per unit.  Tuning: 1 never, n >= 2 force.
+int conv_split_count(long long units, int kblocks, int sm_count) {
+  const int forced = g_tune_conv_splits.load();
+  if (forced == 1) return 1;
+  if (forced >= 2) return forced < kblocks ? forced : (kblocks < 1 ? 1 : kblocks);
+  const long long sms = sm_count > 0 ? sm_count : 148;
+  const long long base = (units + sms - 1) / sms * kblocks;
+  int best = 1;
+  long long best_cost = base;
+  for (int s = 2; s <= 4; ++s) {
+    if (kblocks / s < 8) break;
+    const long long cost = (units * s + sms - 1) / sms * ceil_div(kblocks, s);
+    if (cost * 5 <= base * 4 && cost < best_cost) {
+      best = s;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
+
+// Turns a planned single-CTA conv GEMM (fprop or stride-1 dgrad) into its
+// split-K form writing fp32 partials to `ws`; returns the partial bytes.
+size_t conv_split_bytes(const ConvGemmParams& p, int bn, int splits) {
+  return static_cast<size_t>(splits) * p.sub[0].tiles_m * kBlockM *
+         static_cast<size_t>(p.tiles_n) * bn * sizeof(float);
+}
+
+bool set_conv_split(ConvGemmParams& p, int bn, int splits, void* ws) {
+  const int kb = p.sub[0].rcount * p.sub[0].scount * p.cblocks;
+  p.epi = EPI_PARTIAL;
+  p.conv_split = 1;
+  p.splits = splits;
+  p.kblocks_total = kb;
+  p.tiles_m_total = p.sub[0].tiles_m;
+  p.units = p.sub[0].tiles_m * p.tiles_n * splits;
+  const long long m_pad = static_cast<long long>(p.sub[0].tiles_m) * kBlockM;
+  const int n_pad = p.tiles_n * bn;
+  p.out = ws;
+  p.ws_split_stride = m_pad * n_pad;
+  p.ws_ld = n_pad;
+  p.cin = nullptr;
+  p.bias = nullptr;
+  p.bias_cached = 0;
+  p.use_tma_store = encode_out_2d(&p.mapY, ws, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
+                                  splits * m_pad, n_pad, 16, CU_TENSOR_MAP_SWIZZLE_64B) ? 1 : 0;
+  p.store_box64 = 0;
+  return true;
+}
+
 // Winograd F(2x2, 3x3): output tiles and workspace parts (V [16][T][C],
 // U [K][16][C], M [16][T][K], all 16-bit).
 struct WinoWs {
@@ -976,6 +1030,10 @@ igconv_status_t igconv_set_tuning(igconv_tune_key_t key, int value) {
       if (value < 0 || value > 2) return IGCONV_ERR_INVALID_ARG;
       g_tune_epi_groups.store(value);
       return IGCONV_OK;
+    case IGCONV_TUNE_CONV_SPLITS:
+      if (value < 0 || value > 16) return IGCONV_ERR_INVALID_ARG;
+      g_tune_conv_splits.store(value);
+      return IGCONV_OK;
   }
   return IGCONV_ERR_INVALID_ARG;
 }
@@ -984,8 +1042,18 @@ size_t conv2d_fprop_workspace_size(const igconv_problem_t* prob, igconv_dtype_t 
   int P = 0, Q = 0;
   if (check_shape(prob, &P, &Q) != IGCONV_OK) return 0;
   if (dtype != IGCONV_F16 && dtype != IGCONV_BF16) return 0;
-  if (prob->C > 8) return 0;
-  return few_channel_ws(prob).total;
+  if (prob->C <= 8) return few_channel_ws(prob).total;
+  // split-K partials, when the plan splits (the same decision as conv2d_fprop_ws)
+  const int sms = current_sm_count();
+  const long long tiles_m = ceil_div(static_cast<long long>(prob->N) * P * Q, kBlockM);
+  const int bn = choose_block_n(prob->K, tiles_m, sms);
+  if (bn == 128 && g_tune_no_pairs.load() != 1 && g_tune_conv_splits.load() < 2 && tiles_m >= 2)
+    return 0;  // CTA pairs, no split
+  const int kb = prob->R * prob->S * ceil_div(prob->C, kBlockK);
+  const int splits = conv_split_count(tiles_m * ceil_div(prob->K, bn), kb, sms);
+  if (splits < 2) return 0;
+  return static_cast<size_t>(splits) * tiles_m * kBlockM * static_cast<size_t>(ceil_div(prob->K, bn)) *
+         bn * sizeof(float);
 }
 
 igconv_status_t conv2d_fprop(const igconv_problem_t* prob, igconv_dtype_t dtype, const void* X,
@@ -1047,7 +1115,14 @@ igconv_status_t conv2d_fprop_ws(const igconv_problem_t* prob, igconv_dtype_t dty
   } else if ((st = plan_fprop(p, bn, prob, P, Q, bf16, X, Wt)) != IGCONV_OK) {
     return st;
   }
-  if (!few && use_pairs(bn, p.sub[0].tiles_m, false)) {
+  int splits = 1;
+  if (!few && workspace && !aligned16(workspace)) return IGCONV_ERR_MISALIGNED;
+  if (!few && workspace && !(g_tune_conv_splits.load() < 2 && use_pairs(bn, p.sub[0].tiles_m, false))) {
+    splits = conv_split_count(static_cast<long long>(p.sub[0].tiles_m) * p.tiles_n,
+                              p.sub[0].rcount * p.sub[0].scount * p.cblocks, dev->sm_count);
+    if (splits > 1 && workspace_bytes < conv_split_bytes(p, bn, splits)) return IGCONV_ERR_WORKSPACE;
+  }
+  if (!few && splits == 1 && use_pairs(bn, p.sub[0].tiles_m, false)) {
     // 256-row units; each CTA of a pair loads bn/2 filter rows
     p.pair = 1;
     p.units = ceil_div(p.sub[0].tiles_m, 2) * p.tiles_n;
@@ -1071,6 +1146,14 @@ igconv_status_t conv2d_fprop_ws(const igconv_problem_t* prob, igconv_dtype_t dty
   p.beta = beta;
   p.relu = relu ? 1 : 0;
   p.out_bf16 = bf16;
+  if (splits > 1) {
+    set_conv_split(p, bn, splits, workspace);
+    if (launch_conv_gemm(p, bn, grid_for(p.units, dev), cs) != cudaSuccess) return IGCONV_ERR_CUDA;
+    return from_cuda(launch_conv_splitk_reduce(
+        static_cast<const float*>(workspace), splits, p.ws_split_stride, p.ws_ld,
+        static_cast<long long>(prob->N) * P * Q, prob->K, Y, bf16,
+        beta != 0.0f ? Cin : nullptr, bias, alpha, beta, relu ? 1 : 0, cs));
+  }
   const int grid = p.pair ? grid_for_pairs(p.units, bn, dev) : grid_for(p.units, dev);
   return from_cuda(launch_conv_gemm(p, bn, grid, cs));
 }
@@ -1100,6 +1183,30 @@ static igconv_status_t launch_dgrad_plan(ConvGemmParams& p, int bn, const igconv
 igconv_status_t conv2d_dgrad(const igconv_problem_t* prob, igconv_dtype_t dtype, const void* dY,
                              const void* Wt, const void* Cin, void* dX, float alpha, float beta,
                              void* stream) {
+  return conv2d_dgrad_ws(prob, dtype, dY, Wt, Cin, dX, alpha, beta, nullptr, 0, stream);
+}
+
+size_t conv2d_dgrad_workspace_size(const igconv_problem_t* prob, igconv_dtype_t dtype) {
+  int P = 0, Q = 0;
+  if (check_shape(prob, &P, &Q) != IGCONV_OK) return 0;
+  if (dtype != IGCONV_F16 && dtype != IGCONV_BF16) return 0;
+  if (prob->stride_h != 1 || prob->stride_w != 1) return 0;
+  const int sms = current_sm_count();
+  const long long tiles_m = ceil_div(static_cast<long long>(prob->N) * prob->H * prob->W, kBlockM);
+  const int bn = choose_block_n(prob->C, tiles_m, sms);
+  if (bn == 128 && g_tune_no_pairs.load() != 1 && g_tune_conv_splits.load() < 2 && tiles_m >= 2)
+    return 0;
+  const int kb = prob->R * prob->S * ceil_div(prob->K, kBlockK);
+  const int splits = conv_split_count(tiles_m * ceil_div(prob->C, bn), kb, sms);
+  if (splits < 2) return 0;
+  return static_cast<size_t>(splits) * tiles_m * kBlockM * static_cast<size_t>(ceil_div(prob->C, bn)) *
+         bn * sizeof(float);
+}
+
+igconv_status_t conv2d_dgrad_ws(const igconv_problem_t* prob, igconv_dtype_t dtype,
+                                const void* dY, const void* Wt, const void* Cin, void* dX,
+                                float alpha, float beta, void* workspace, size_t workspace_bytes,
+                                void* stream) {
   int P = 0, Q = 0;
   igconv_status_t st = check_shape(prob, &P, &Q);
   if (st != IGCONV_OK) return st;
@@ -1117,6 +1224,27 @@ igconv_status_t conv2d_dgrad(const igconv_problem_t* prob, igconv_dtype_t dtype,
   int bn = 0;
   const int bf16 = dtype == IGCONV_BF16 ? 1 : 0;
   if ((st = plan_dgrad(p, &bn, prob, P, Q, bf16, dY, Wt, dev->sm_count)) != IGCONV_OK) return st;
+  if (workspace && !aligned16(workspace)) return IGCONV_ERR_MISALIGNED;
+  const bool unit_stride = prob->stride_h == 1 && prob->stride_w == 1 && p.nsub == 1;
+  int splits = 1;
+  if (workspace && unit_stride &&
+      !(g_tune_conv_splits.load() < 2 && use_pairs(bn, p.sub[0].tiles_m, true))) {
+    splits = conv_split_count(static_cast<long long>(p.sub[0].tiles_m) * p.tiles_n,
+                              p.sub[0].rcount * p.sub[0].scount * p.cblocks, dev->sm_count);
+    if (splits > 1 && workspace_bytes < conv_split_bytes(p, bn, splits)) return IGCONV_ERR_WORKSPACE;
+  }
+  if (splits > 1) {
+    set_conv_split(p, bn, splits, workspace);
+    p.alpha = 1.0f;
+    p.pf_base = Wt;
+    p.pf_bytes = static_cast<long long>(prob->K) * prob->R * prob->S * prob->C * 2;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (launch_conv_gemm(p, bn, grid_for(p.units, dev), cs) != cudaSuccess) return IGCONV_ERR_CUDA;
+    return from_cuda(launch_conv_splitk_reduce(
+        static_cast<const float*>(workspace), splits, p.ws_split_stride, p.ws_ld,
+        static_cast<long long>(prob->N) * prob->H * prob->W, prob->C, dX, bf16,
+        beta != 0.0f ? Cin : nullptr, nullptr, alpha, beta, 0, cs));
+  }
   if (p.nsub == 1 && p.sub[0].tile_begin == 0 && use_pairs(bn, p.sub[0].tiles_m, true)) {
     // 256-row units; each CTA of a pair loads one 64-column half of the filter tile
     p.pair = 1;

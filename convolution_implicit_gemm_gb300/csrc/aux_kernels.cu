@@ -514,6 +514,106 @@ cudaError_t launch_wgrad_reduce(const float* ws, int splits, long long split_str
 }
 
 // ---------------------------------------------------------------------------
+// Split-K convolution (fprop, stride-1 dgrad): out[m][n] = cast(relu?(alpha *
+// sum_s ws[s][m][n] + beta * cin[m][n] + bias[n])), the splits added in split
+// order (deterministic), then fprop's epilogue in the same order as the
+// GEMM's own (alpha, beta * Cin, bias, ReLU, round to nearest even).  One
+// thread per 8 consecutive columns (16 output bytes); cols % 8 == 0.
+// ---------------------------------------------------------------------------
+// 8 packed 16-bit values -> fp32, and a pair of fp32 -> packed 16 bits
+// (round to nearest even, x in the low half).
+__device__ __forceinline__ void unpack_row8(uint4 r, float (&f)[8], int bf16) {
+  const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t lo = w[i] & 0xFFFFu, hi = w[i] >> 16;
+    if (bf16) {
+      f[2 * i] = __uint_as_float(lo << 16);
+      f[2 * i + 1] = __uint_as_float(hi << 16);
+    } else {
+      f[2 * i] = __half2float(__ushort_as_half(static_cast<unsigned short>(lo)));
+      f[2 * i + 1] = __half2float(__ushort_as_half(static_cast<unsigned short>(hi)));
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_pair16(float a, float b, int bf16) {
+  if (bf16) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&v);
+  }
+  const __half2 v = __floats2half2_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__global__ void __launch_bounds__(256) conv_splitk_reduce_kernel(
+    const float* __restrict__ ws, int splits, long long split_stride, int ws_ld, long long rows,
+    int cols, uint4* __restrict__ out, int out_bf16, const uint4* __restrict__ cin,
+    const uint4* __restrict__ bias, float alpha, float beta, int relu) {
+  const int c8 = cols / 8;
+  const long long total = rows * c8;
+  for (long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
+       e += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long m = e / c8;
+    const int n = static_cast<int>(e - m * c8) * 8;
+    const float* src = ws + m * ws_ld + n;
+    float v[8];
+    {
+      const float4 a = __ldcs(reinterpret_cast<const float4*>(src));
+      const float4 b = __ldcs(reinterpret_cast<const float4*>(src + 4));
+      v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+      v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+    for (int sp = 1; sp < splits; ++sp) {
+      const float* q = src + static_cast<long long>(sp) * split_stride;
+      const float4 a = __ldcs(reinterpret_cast<const float4*>(q));
+      const float4 b = __ldcs(reinterpret_cast<const float4*>(q + 4));
+      v[0] = __fadd_rn(v[0], a.x); v[1] = __fadd_rn(v[1], a.y);
+      v[2] = __fadd_rn(v[2], a.z); v[3] = __fadd_rn(v[3], a.w);
+      v[4] = __fadd_rn(v[4], b.x); v[5] = __fadd_rn(v[5], b.y);
+      v[6] = __fadd_rn(v[6], b.z); v[7] = __fadd_rn(v[7], b.w);
+    }
+    float cv[8] = {0, 0, 0, 0, 0, 0, 0, 0}, bv[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    if (beta != 0.0f) {
+      const uint4 r = cin[e];
+      unpack_row8(r, cv, out_bf16);
+    }
+    if (bias) unpack_row8(bias[n / 8], bv, out_bf16);
+    uint32_t pk[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float x0 = __fmul_rn(alpha, v[2 * i]), x1 = __fmul_rn(alpha, v[2 * i + 1]);
+      if (beta != 0.0f) {
+        x0 = __fmaf_rn(beta, cv[2 * i], x0);
+        x1 = __fmaf_rn(beta, cv[2 * i + 1], x1);
+      }
+      x0 = __fadd_rn(x0, bv[2 * i]);
+      x1 = __fadd_rn(x1, bv[2 * i + 1]);
+      if (relu) {
+        x0 = fmaxf(x0, 0.0f);
+        x1 = fmaxf(x1, 0.0f);
+      }
+      pk[i] = pack_pair16(x0, x1, out_bf16);
+    }
+    out[e] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  }
+}
+
+cudaError_t launch_conv_splitk_reduce(const float* ws, int splits, long long split_stride,
+                                      int ws_ld, long long rows, int cols, void* out,
+                                      int out_bf16, const void* cin, const void* bias,
+                                      float alpha, float beta, int relu, cudaStream_t s) {
+  const long long total = rows * (cols / 8);
+  long long blocks = (total + 255) / 256;
+  if (blocks < 1) blocks = 1;
+  if (blocks > 65536) blocks = 65536;
+  conv_splitk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+      ws, splits, split_stride, ws_ld, rows, cols, static_cast<uint4*>(out), out_bf16,
+      static_cast<const uint4*>(cin), static_cast<const uint4*>(bias), alpha, beta, relu);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
 // int8 wgrad: dW[k][rs][c] (int32) = the sum of the int32 partial tiles of
 // the splits, wrapping modulo 2^32 like the int32 accumulator they stand for
 // (exact and order-independent).  One thread per element of the partial matrix, so the reads of

@@ -87,6 +87,7 @@ struct Work {
 // role (kernel-parameter loads through a reference are slow in hot loops).
 struct Sched {
   int epi, units, tiles_m_total, tiles_n, splits, kblocks_total, nsub, cblocks;
+  int conv;  // operands are the convolution's (fprop / dgrad), not wgrad's
   int pair;  // CTA pairs: a unit is 256 rows, this CTA takes the half of its rank
   int rank;  // this CTA's rank in its pair (0 without pairs)
 };
@@ -95,6 +96,7 @@ template <bool PAIR>
 __device__ __forceinline__ Sched load_sched(const ConvGemmParams& p) {
   Sched s;
   s.epi = p.epi;
+  s.conv = p.epi != EPI_PARTIAL || p.conv_split;
   s.units = p.units;
   s.tiles_m_total = p.tiles_m_total;
   s.tiles_n = p.tiles_n;
@@ -238,7 +240,7 @@ template <bool VOL>
 __device__ __forceinline__ void producer_enter_unit(const ConvGemmParams& p, const ProdCtx& c,
                                                     ProducerPos& s) {
   s.w = decode_unit(p, c.sc, s.u);
-  if (c.sc.epi != EPI_PARTIAL) {
+  if (c.sc.conv) {
     const SubProblem& sp = p.sub[s.w.sub];
     const int Hs = sp.Hs, Ws = sp.Ws;
     const int m0 = s.w.tile_m * kBlockM;
@@ -346,7 +348,7 @@ __device__ __forceinline__ void issue_stage_loads(const ProdCtx& c, const Produc
     }
     return;
   }
-  if (c.sc.epi != EPI_PARTIAL) {
+  if (c.sc.conv) {
     // reduction block kb = (tap, 64-channel block)
     const int tap = kb / c.sc.cblocks;
     const int cb = kb - tap * c.sc.cblocks;

@@ -125,6 +125,8 @@ struct ConvGemmParams {
   int epi_groups;             // epilogue warp groups: 0 or 2 two groups of four taking
                               // alternate tiles whole (four TMEM buffers) where they fit,
                               // 1 one group of eight warps per tile (two buffers)
+  int conv_split;             // 1 with EPI_PARTIAL: split-K over a convolution (fprop or
+                              // stride-1 dgrad): conv operand loads, fp32 partial tiles
   int int_acc;                // 1: the accumulators hold exact integers (int8 operands on the
                               // fp16 path); EPI_STORE writes their int32 sum, EPI_PARTIAL
                               // int32 partial sums (int8 dgrad / wgrad)
@@ -145,6 +147,10 @@ cudaError_t launch_wgrad_reduce(const float* ws, int splits, long long split_str
                                 int rows, int cols, int swapped, int K, int RS, int C, int cpad,
                                 void* dW, int dw_dtype, const void* cin, float alpha, float beta,
                                 cudaStream_t s);
+cudaError_t launch_conv_splitk_reduce(const float* ws, int splits, long long split_stride,
+                                      int ws_ld, long long rows, int cols, void* out,
+                                      int out_bf16, const void* cin, const void* bias,
+                                      float alpha, float beta, int relu, cudaStream_t s);
 cudaError_t launch_wgrad_reduce_i32(const int* ws, int splits, long long split_stride, int ws_ld,
                                     int rows, int cols, int swapped, int K, int RS, int C,
                                     int cpad, int* dW, cudaStream_t s);

@@ -117,9 +117,11 @@ IGCONV_API igconv_status_t conv2d_fprop(const igconv_problem_t *prob, igconv_dty
                                         const void *Cin, void *Y, float alpha, float beta,
                                         int relu, void *stream);
 
-/* Bytes of device workspace conv2d_fprop_ws needs for this problem: nonzero
- * only for C <= 8 (the few-channel path), 0 for an invalid problem or dtype.
- * Host only. */
+/* Bytes of device workspace conv2d_fprop_ws needs for this problem: for C
+ * <= 8 the few-channel copies; for larger C the split-K partial tiles when
+ * the plan splits the reduction (see conv2d_fprop_ws), else 0.  0 for an
+ * invalid problem or dtype.  Host only; queried on the current device (the
+ * split choice depends on its SM count). */
 IGCONV_API size_t conv2d_fprop_workspace_size(const igconv_problem_t *prob,
                                               igconv_dtype_t dtype);
 
@@ -128,15 +130,24 @@ IGCONV_API size_t conv2d_fprop_workspace_size(const igconv_problem_t *prob,
  * stride 2).  The same result definition as conv2d_fprop.  The path copies
  * the pixels to 8-channel rows (zero channels C..7; skipped when C == 8) and
  * the filter to a [R*S][K][8] layout in the workspace, and packs 8 filter
- * taps x 8 channels into each 64-deep reduction block.  With C > 8 the
- * workspace is not used (it may be NULL).
+ * taps x 8 channels into each 64-deep reduction block.
+ * With C > 8 and a workspace, a layer whose whole tiles would leave the last
+ * wave of persistent CTAs mostly empty (e.g. 7x7 512 -> 512 at batch 128:
+ * 98 tiles on 152 SMs) runs split-K: each tile's reduction is cut into 2-4
+ * equal ranges on separate CTAs, which write fp32 partial tiles to the
+ * workspace; a second kernel adds them in split order (deterministic) and
+ * applies alpha, beta * Cin, bias, ReLU and the cast.  The sums are then
+ * grouped differently from the unsplit path (exact on integer data, within
+ * the fp32 accumulation bound otherwise).  Without a workspace (or when the
+ * size query returns 0) the layer runs unsplit.
  *   workspace        device memory, 16-byte aligned, at least
  *                    conv2d_fprop_workspace_size(prob, dtype) bytes; it must
  *                    stay untouched until the call's kernels have run
  *   X, Wt            2-byte aligned for C < 8 (16-byte for C == 8); the
  *                    other arguments as in conv2d_fprop
  * Errors: as conv2d_fprop; WORKSPACE if C < 8 and the workspace is NULL or
- * too small (or C == 8 with a non-NULL workspace that is too small). */
+ * too small (or C == 8 with a non-NULL workspace that is too small, or a
+ * split plan with a workspace that is too small). */
 IGCONV_API igconv_status_t conv2d_fprop_ws(const igconv_problem_t *prob, igconv_dtype_t dtype,
                                            const void *X, const void *Wt, const void *bias,
                                            const void *Cin, void *Y, float alpha, float beta,
@@ -159,6 +170,21 @@ IGCONV_API igconv_status_t conv2d_fprop_ws(const igconv_problem_t *prob, igconv_
 IGCONV_API igconv_status_t conv2d_dgrad(const igconv_problem_t *prob, igconv_dtype_t dtype,
                                         const void *dY, const void *Wt, const void *Cin,
                                         void *dX, float alpha, float beta, void *stream);
+
+/* conv2d_dgrad with a caller-owned device workspace, which lets a unit-
+ * stride layer whose tiles leave the last wave mostly empty run split-K
+ * exactly as conv2d_fprop_ws does (fp32 partials in the workspace, an
+ * ordered reduction applying alpha and beta * Cin).  The size query returns
+ * 0 (no workspace needed) for strided problems and unsplit plans; it is
+ * host-only and queried on the current device.  Arguments, errors and the
+ * result definition as conv2d_dgrad; WORKSPACE when a split plan's
+ * workspace is too small. */
+IGCONV_API size_t conv2d_dgrad_workspace_size(const igconv_problem_t *prob,
+                                              igconv_dtype_t dtype);
+IGCONV_API igconv_status_t conv2d_dgrad_ws(const igconv_problem_t *prob, igconv_dtype_t dtype,
+                                           const void *dY, const void *Wt, const void *Cin,
+                                           void *dX, float alpha, float beta, void *workspace,
+                                           size_t workspace_bytes, void *stream);
 
 /* Bytes of device workspace conv2d_wgrad needs for this problem (fp32
  * split-K partial sums).  The split count depends on the SM count of the
@@ -518,13 +544,19 @@ IGCONV_API const char *igconv_status_string(igconv_status_t status);
  *                             with four TMEM buffers; 1: one group of eight
  *                             warps per tile, two buffers.  Results are
  *                             bit-identical.
+ *   IGCONV_TUNE_CONV_SPLITS   split-K of conv2d_fprop_ws / conv2d_dgrad_ws
+ *                             (when given a workspace): 0 the built-in
+ *                             choice, 1 never, n >= 2 always n (at most 16,
+ *                             clamped to the reduction blocks; CTA pairs
+ *                             are then not used).
  * Returns INVALID_ARG for an unknown key or value. */
 typedef enum {
     IGCONV_TUNE_WGRAD_SPLITS = 1,
     IGCONV_TUNE_BLOCK_N = 2,
     IGCONV_TUNE_MAX_CTAS = 3,
     IGCONV_TUNE_CTA_PAIRS = 4,
-    IGCONV_TUNE_EPI_GROUPS = 5
+    IGCONV_TUNE_EPI_GROUPS = 5,
+    IGCONV_TUNE_CONV_SPLITS = 6
 } igconv_tune_key_t;
 IGCONV_API igconv_status_t igconv_set_tuning(igconv_tune_key_t key, int value);
 
