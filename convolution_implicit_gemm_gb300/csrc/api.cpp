@@ -907,28 +907,20 @@ void plan_wgrad_int8(const igconv_problem_t* pb, int P, int Q, int sm_count, Wgr
 }
 
 // Split-K for the forward and stride-1 data passes (single sub-problem,
-// single CTAs): when whole tiles leave the last wave of persistent CTAs
-// mostly empty, each tile's reduction is cut into `splits` equal ranges and
-// the fp32 partial tiles are added in order by a reduction that also applies
-// the epilogue.  Model: waves x blocks per unit; a split must save at least
-// a fifth of that and keep 8 blocks per unit.  Tuning: 1 never, n >= 2 force.
+// single CTAs): each tile's reduction cut into `splits` equal ranges whose
+// fp32 partial tiles an ordered reduction adds, applying the epilogue.  It
+// runs only when forced by the tuning knob (n >= 2): measured on the
+// ResNet-50 layers at batch 128 it loses everywhere, also where whole tiles
+// leave most of the last wave empty (7x7 512 -> 512: 98 tiles on 152 SMs,
+// 36.5 us unsplit against 38.5 / 42.7 / 42.3 us with 3 / 2 / 4 splits; 14x14
+// and 28x28: 1.5-2.7x slower), because the partial tiles' round trip and
+// the reduction cost more than the wave they recover.
 int conv_split_count(long long units, int kblocks, int sm_count) {
+  (void)units;
+  (void)sm_count;
   const int forced = g_tune_conv_splits.load();
-  if (forced == 1) return 1;
   if (forced >= 2) return forced < kblocks ? forced : (kblocks < 1 ? 1 : kblocks);
-  const long long sms = sm_count > 0 ? sm_count : 148;
-  const long long base = (units + sms - 1) / sms * kblocks;
-  int best = 1;
-  long long best_cost = base;
-  for (int s = 2; s <= 4; ++s) {
-    if (kblocks / s < 8) break;
-    const long long cost = (units * s + sms - 1) / sms * ceil_div(kblocks, s);
-    if (cost * 5 <= base * 4 && cost < best_cost) {
-      best = s;
-      best_cost = cost;
-    }
-  }
-  return best;
+  return 1;
 }
 
 // Turns a planned single-CTA conv GEMM (fprop or stride-1 dgrad) into its

@@ -131,15 +131,15 @@ IGCONV_API size_t conv2d_fprop_workspace_size(const igconv_problem_t *prob,
  * the pixels to 8-channel rows (zero channels C..7; skipped when C == 8) and
  * the filter to a [R*S][K][8] layout in the workspace, and packs 8 filter
  * taps x 8 channels into each 64-deep reduction block.
- * With C > 8 and a workspace, a layer whose whole tiles would leave the last
- * wave of persistent CTAs mostly empty (e.g. 7x7 512 -> 512 at batch 128:
- * 98 tiles on 152 SMs) runs split-K: each tile's reduction is cut into 2-4
+ * With C > 8 and a workspace, the layer can run split-K when the tuning
+ * knob IGCONV_TUNE_CONV_SPLITS asks for it: each tile's reduction cut into
  * equal ranges on separate CTAs, which write fp32 partial tiles to the
  * workspace; a second kernel adds them in split order (deterministic) and
  * applies alpha, beta * Cin, bias, ReLU and the cast.  The sums are then
  * grouped differently from the unsplit path (exact on integer data, within
- * the fp32 accumulation bound otherwise).  Without a workspace (or when the
- * size query returns 0) the layer runs unsplit.
+ * the fp32 accumulation bound otherwise).  The built-in plan never splits
+ * (measured slower on every layer tried), so by default the size query
+ * returns 0 for C > 8 and the layer runs exactly as conv2d_fprop.
  *   workspace        device memory, 16-byte aligned, at least
  *                    conv2d_fprop_workspace_size(prob, dtype) bytes; it must
  *                    stay untouched until the call's kernels have run
@@ -172,11 +172,11 @@ IGCONV_API igconv_status_t conv2d_dgrad(const igconv_problem_t *prob, igconv_dty
                                         void *dX, float alpha, float beta, void *stream);
 
 /* conv2d_dgrad with a caller-owned device workspace, which lets a unit-
- * stride layer whose tiles leave the last wave mostly empty run split-K
- * exactly as conv2d_fprop_ws does (fp32 partials in the workspace, an
- * ordered reduction applying alpha and beta * Cin).  The size query returns
- * 0 (no workspace needed) for strided problems and unsplit plans; it is
- * host-only and queried on the current device.  Arguments, errors and the
+ * stride layer run split-K as conv2d_fprop_ws does (fp32 partials in the
+ * workspace, an ordered reduction applying alpha and beta * Cin) when the
+ * tuning knob IGCONV_TUNE_CONV_SPLITS asks for it.  The size query returns 0
+ * (no workspace needed) for strided problems and unsplit plans, which by
+ * default is every plan; it is host-only and queried on the current device.  Arguments, errors and the
  * result definition as conv2d_dgrad; WORKSPACE when a split plan's
  * workspace is too small. */
 IGCONV_API size_t conv2d_dgrad_workspace_size(const igconv_problem_t *prob,
@@ -545,8 +545,8 @@ IGCONV_API const char *igconv_status_string(igconv_status_t status);
  *                             warps per tile, two buffers.  Results are
  *                             bit-identical.
  *   IGCONV_TUNE_CONV_SPLITS   split-K of conv2d_fprop_ws / conv2d_dgrad_ws
- *                             (when given a workspace): 0 the built-in
- *                             choice, 1 never, n >= 2 always n (at most 16,
+ *                             (when given a workspace): 0 or 1 never (the
+ *                             built-in choice), n >= 2 always n (at most 16,
  *                             clamped to the reduction blocks; CTA pairs
  *                             are then not used).
  * Returns INVALID_ARG for an unknown key or value. */
