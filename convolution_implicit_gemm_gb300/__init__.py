@@ -628,7 +628,13 @@ def dgrad(prob, dY, Wt, Cin=None, alpha=1.0, beta=0.0, out=None, stream=None):
     pb = Problem.make(prob)
     dX = out if out is not None else torch.empty((pb.N, pb.H, pb.W, pb.C), dtype=dY.dtype,
                                                  device=dY.device)
-    conv2d_dgrad(pb, dY.dtype, dY, Wt, Cin, dX, alpha, beta, stream)
+    if pb.C < 8:
+        # the few-channel path and its workspace (padded filter, fp32 rows)
+        ws = torch.empty(max(conv2d_dgrad_workspace_size(pb, dY.dtype), 16), dtype=torch.uint8,
+                         device=dY.device)
+        conv2d_dgrad_ws(pb, dY.dtype, dY, Wt, Cin, dX, alpha, beta, ws, stream=stream)
+    else:
+        conv2d_dgrad(pb, dY.dtype, dY, Wt, Cin, dX, alpha, beta, stream)
     return dX
 
 

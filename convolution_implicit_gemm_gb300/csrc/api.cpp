@@ -548,21 +548,16 @@ struct WgradPlan {
 // rows), the tile width and the split count are chosen together, minimising
 // (waves of persistent CTAs) x (columns x reduction blocks per unit) / (tile
 // efficiency).  Splits fill at most one wave and keep >= 8 blocks each.
-void plan_wgrad_shape(const igconv_problem_t* pb, int P, int Q, int sm_count, WgradPlan* w,
-                      int max_bn = 256) {
+// Orientation, tile width and split count of a wgrad GEMM with an X side of
+// `xext` rows (the (tap, c) extent) and the dY side of K rows.
+void choose_wgrad_shape(int K, long long xext, int sm_count, WgradPlan* w, int max_bn) {
   const int sms = sm_count > 0 ? sm_count : 148;
-  w->rs = pb->R * pb->S;
-  w->cblocks = ceil_div(pb->C, kBlockK);
-  w->cpad = w->cblocks * kBlockK;
-  const long long xext = static_cast<long long>(w->rs) * w->cpad;
-  const long long npq = static_cast<long long>(pb->N) * P * Q;
-  w->kblocks = ceil_div(npq, kBlockK);
   const int forced_splits = g_tune_splits.load();
   const int forced_bn = g_tune_bn.load();
   double best = 1e300;
   for (int swapped = 0; swapped < 2; ++swapped) {
-    const long long mext = swapped ? pb->K : xext;
-    const long long next = swapped ? xext : pb->K;
+    const long long mext = swapped ? K : xext;
+    const long long next = swapped ? xext : K;
     const int cands[3] = {256, 128, 64};
     for (int bn : cands) {
       if (forced_bn && bn != forced_bn) continue;
@@ -595,6 +590,28 @@ void plan_wgrad_shape(const igconv_problem_t* pb, int P, int Q, int sm_count, Wg
   w->M_pad = w->tiles_m * kBlockM;
   w->N_pad = w->tiles_n * w->bn;
   w->ws_bytes = static_cast<size_t>(w->splits) * w->M_pad * w->N_pad * sizeof(float);
+}
+
+void plan_wgrad_shape(const igconv_problem_t* pb, int P, int Q, int sm_count, WgradPlan* w,
+                      int max_bn = 256) {
+  w->rs = pb->R * pb->S;
+  w->cblocks = ceil_div(pb->C, kBlockK);
+  w->cpad = w->cblocks * kBlockK;
+  const long long npq = static_cast<long long>(pb->N) * P * Q;
+  w->kblocks = ceil_div(npq, kBlockK);
+  choose_wgrad_shape(pb->K, static_cast<long long>(w->rs) * w->cpad, sm_count, w, max_bn);
+}
+
+// Few channels (C < 8, pixels padded to 8): the X side is tap-packed, 8
+// taps x 8 channels per 64-row chunk, so row = tap * 8 + c (channel pitch 8)
+// and a 7x7 filter needs 7 chunks (448 rows) instead of 49.
+void plan_wgrad_taps(const igconv_problem_t* pb, int P, int Q, int sm_count, WgradPlan* w) {
+  w->rs = pb->R * pb->S;
+  w->cblocks = 1;
+  w->cpad = 8;
+  const long long npq = static_cast<long long>(pb->N) * P * Q;
+  w->kblocks = ceil_div(npq, kBlockK);
+  choose_wgrad_shape(pb->K, static_cast<long long>(ceil_div(w->rs, 8)) * kBlockK, sm_count, w, 256);
 }
 
 // Grouped wgrad as a block-diagonal GEMM (C == K, group width 4..64): rows
@@ -952,6 +969,103 @@ bool set_conv_split(ConvGemmParams& p, int bn, int splits, void* ws) {
   return true;
 }
 
+// Few-channel dgrad (C < 8): the filter padded to 8 channels and the fp32
+// result rows of 8 channels, both in the workspace.
+struct FewDgradWs {
+  size_t w_bytes, x_bytes, total;
+};
+FewDgradWs few_dgrad_ws(const igconv_problem_t* pb) {
+  FewDgradWs w;
+  w.w_bytes = round256(static_cast<size_t>(pb->K) * pb->R * pb->S * 16);
+  w.x_bytes = round256(static_cast<size_t>(pb->N) * pb->H * pb->W * 8 * sizeof(float));
+  w.total = w.w_bytes + w.x_bytes;
+  return w;
+}
+
+// Few-channel wgrad (C < 8): the pixels copied to 8-channel rows in the
+// workspace, then the wgrad GEMM with a tap-packed X side (8 taps x 8
+// channels per 64-row chunk, row = tap * 8 + c) and the usual ordered
+// split reduction, which writes the C real channels of each tap.
+igconv_status_t wgrad_few_channels(const igconv_problem_t* prob, int P, int Q,
+                                   igconv_dtype_t dtype, igconv_dtype_t dw_dtype, const void* X,
+                                   const void* dY, const void* Cin, void* dW, float alpha,
+                                   float beta, void* workspace, size_t workspace_bytes,
+                                   void* stream) {
+  igconv_problem_t k8 = *prob;
+  k8.C = 8;
+  igconv_status_t st = check_limits(&k8, P, Q, 8);
+  if (st != IGCONV_OK) return st;
+  const uintptr_t esz = dw_dtype == IGCONV_F32 ? 4 : 2;
+  if ((reinterpret_cast<uintptr_t>(X) & 1) || !aligned16(dY) ||
+      (reinterpret_cast<uintptr_t>(dW) & (esz - 1)) ||
+      (beta != 0.0f && (reinterpret_cast<uintptr_t>(Cin) & (esz - 1))) ||
+      (workspace && !aligned16(workspace)))
+    return IGCONV_ERR_MISALIGNED;
+  DeviceState* dev = nullptr;
+  if ((st = device_state(&dev)) != IGCONV_OK) return st;
+  WgradPlan w;
+  plan_wgrad_taps(prob, P, Q, dev->sm_count, &w);
+  const long long pixels = static_cast<long long>(prob->N) * prob->H * prob->W;
+  const size_t x8_bytes = round256(static_cast<size_t>(pixels) * 16);
+  if (!workspace || workspace_bytes < x8_bytes + w.ws_bytes) return IGCONV_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* X8 = ws;
+  void* part = ws + x8_bytes;
+  const int bf16 = dtype == IGCONV_BF16 ? 1 : 0;
+  const long long xext = static_cast<long long>(ceil_div(w.rs, 8)) * kBlockK;
+  ConvGemmParams p;
+  init_common(p, dev);
+  p.nsub = 1;
+  p.a_src = w.swapped ? SRC_2D_MN : SRC_IM2COL_TAPS_MN;
+  p.b_src = w.swapped ? SRC_IM2COL_TAPS_MN : SRC_2D_MN;
+  p.epi = EPI_PARTIAL;
+  p.tiles_m_total = w.tiles_m;
+  p.tiles_n = w.tiles_n;
+  p.splits = w.splits;
+  p.kblocks_total = w.kblocks;
+  p.units = w.tiles_m * w.tiles_n * w.splits;
+  p.cblocks = 1;
+  p.N_gemm = w.N_pad;
+  p.idesc = make_idesc(kBlockM, w.bn, bf16, 1, 1);
+  set_fp_accumulators(p, w.bn);
+  p.wg_PQ = P * Q;
+  p.wg_Q = Q;
+  p.wg_lower_h = -prob->pad_h;
+  p.wg_lower_w = -prob->pad_w;
+  p.wg_sh = prob->stride_h;
+  p.wg_sw = prob->stride_w;
+  p.wg_S = prob->S;
+  p.wg_RS = w.rs;
+  p.wg_dh = prob->dil_h;
+  p.wg_dw = prob->dil_w;
+  p.wg_K = prob->K;
+  p.out = part;
+  p.ws_split_stride = static_cast<long long>(w.M_pad) * w.N_pad;
+  p.ws_ld = w.N_pad;
+  p.use_tma_store = encode_out_2d(&p.mapY, part, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
+                                  static_cast<long long>(w.splits) * w.M_pad, w.N_pad, 16,
+                                  CU_TENSOR_MAP_SWIZZLE_64B) ? 1 : 0;
+  // 64 output positions x 8 channels (16 bytes each) per load, no swizzle
+  if (!encode_im2col(&p.mapA[0], X8, bf16, prob->N, prob->H, prob->W, 8, -prob->pad_h,
+                     -prob->pad_w, prob->pad_h - (prob->R - 1) * prob->dil_h,
+                     prob->pad_w - (prob->S - 1) * prob->dil_w, prob->stride_h, prob->stride_w,
+                     kBlockK, 8, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return IGCONV_ERR_UNSUPPORTED;
+  p.mapA_valid = 1u;
+  const long long npq = static_cast<long long>(prob->N) * P * Q;
+  if (!encode_2d(&p.mapB, dY, bf16, npq, prob->K)) return IGCONV_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (launch_pad_pixels8(X, X8, pixels, prob->C, s) != cudaSuccess) return IGCONV_ERR_CUDA;
+  if (launch_conv_gemm(p, w.bn, grid_for(p.units, dev), s) != cudaSuccess) return IGCONV_ERR_CUDA;
+  const int dwt = dw_dtype == IGCONV_F32 ? 2 : (dw_dtype == IGCONV_BF16 ? 1 : 0);
+  return from_cuda(launch_wgrad_reduce(static_cast<const float*>(part), w.splits,
+                                       p.ws_split_stride, w.N_pad,
+                                       static_cast<int>(w.swapped ? prob->K : xext),
+                                       static_cast<int>(w.swapped ? xext : prob->K), w.swapped,
+                                       prob->K, w.rs, prob->C, 8, dW, dwt,
+                                       beta != 0.0f ? Cin : nullptr, alpha, beta, s));
+}
+
 // Winograd F(2x2, 3x3): output tiles and workspace parts (V [16][T][C],
 // U [K][16][C], M [16][T][K], all 16-bit).
 struct WinoWs {
@@ -1182,6 +1296,7 @@ size_t conv2d_dgrad_workspace_size(const igconv_problem_t* prob, igconv_dtype_t 
   int P = 0, Q = 0;
   if (check_shape(prob, &P, &Q) != IGCONV_OK) return 0;
   if (dtype != IGCONV_F16 && dtype != IGCONV_BF16) return 0;
+  if (prob->C < 8) return few_dgrad_ws(prob).total;
   if (prob->stride_h != 1 || prob->stride_w != 1) return 0;
   const int sms = current_sm_count();
   const long long tiles_m = ceil_div(static_cast<long long>(prob->N) * prob->H * prob->W, kBlockM);
@@ -1205,6 +1320,49 @@ igconv_status_t conv2d_dgrad_ws(const igconv_problem_t* prob, igconv_dtype_t dty
   if (!dY || !Wt || !dX || (beta != 0.0f && !Cin)) return IGCONV_ERR_INVALID_ARG;
   if (!std::isfinite(alpha) || !std::isfinite(beta)) return IGCONV_ERR_INVALID_ARG;
   if (dtype != IGCONV_F16 && dtype != IGCONV_BF16) return IGCONV_ERR_UNSUPPORTED;
+  if (prob->C < 8) {
+    // few input channels: the dense dgrad over the filter padded to 8
+    // channels, alpha * acc written as fp32 rows of 8 channels, then the C
+    // real channels finished with beta * Cin and the cast
+    igconv_problem_t k8 = *prob;
+    k8.C = 8;
+    if ((st = check_limits(&k8, P, Q, 8)) != IGCONV_OK) return st;
+    if (prob->stride_h * prob->stride_w > kMaxSub) return IGCONV_ERR_UNSUPPORTED;
+    if (!aligned16(dY) || (reinterpret_cast<uintptr_t>(Wt) & 1) ||
+        (reinterpret_cast<uintptr_t>(dX) & 1) ||
+        (beta != 0.0f && (reinterpret_cast<uintptr_t>(Cin) & 1)) ||
+        (workspace && !aligned16(workspace)))
+      return IGCONV_ERR_MISALIGNED;
+    const FewDgradWs fw = few_dgrad_ws(prob);
+    if (!workspace || workspace_bytes < fw.total) return IGCONV_ERR_WORKSPACE;
+    DeviceState* dev = nullptr;
+    if ((st = device_state(&dev)) != IGCONV_OK) return st;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    void* W8 = ws;
+    float* dX8 = reinterpret_cast<float*>(ws + fw.w_bytes);
+    const int bf16 = dtype == IGCONV_BF16 ? 1 : 0;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (launch_pad_pixels8(Wt, W8, static_cast<long long>(prob->K) * prob->R * prob->S, prob->C,
+                           cs) != cudaSuccess)
+      return IGCONV_ERR_CUDA;
+    ConvGemmParams p;
+    init_common(p, dev);
+    int bn = 0;
+    if ((st = plan_dgrad(p, &bn, &k8, P, Q, bf16, dY, W8, dev->sm_count)) != IGCONV_OK) return st;
+    p.epi = EPI_STORE;
+    p.out_f32 = 1;
+    p.out = dX8;
+    p.use_tma_store = 0;
+    p.alpha = alpha;
+    p.out_bf16 = bf16;
+    p.pf_base = W8;
+    p.pf_bytes = static_cast<long long>(prob->K) * prob->R * prob->S * 16;
+    if (p.units > 0 && launch_conv_gemm(p, bn, grid_for(p.units, dev), cs) != cudaSuccess)
+      return IGCONV_ERR_CUDA;
+    return from_cuda(launch_unpad_channels(dX8, dX,
+                                           static_cast<long long>(prob->N) * prob->H * prob->W,
+                                           prob->C, bf16, beta != 0.0f ? Cin : nullptr, beta, cs));
+  }
   if ((st = check_limits(prob, P, Q, 8)) != IGCONV_OK) return st;
   if (prob->stride_h * prob->stride_w > kMaxSub) return IGCONV_ERR_UNSUPPORTED;
   if (!aligned16(dY) || !aligned16(Wt) || !aligned16(dX) || (beta != 0.0f && !aligned16(Cin)))
@@ -1265,6 +1423,10 @@ size_t conv2d_wgrad_workspace_size(const igconv_problem_t* prob, igconv_dtype_t 
     cudaGetLastError();  // no device: size for the default SM count
   }
   WgradPlan w;
+  if (prob->C < 8) {  // few channels: the 8-channel pixel copy, then the partials
+    plan_wgrad_taps(prob, P, Q, sm_count, &w);
+    return round256(static_cast<size_t>(prob->N) * prob->H * prob->W * 16) + w.ws_bytes;
+  }
   plan_wgrad_shape(prob, P, Q, sm_count, &w);
   return w.ws_bytes;
 }
@@ -1281,6 +1443,8 @@ igconv_status_t conv2d_wgrad(const igconv_problem_t* prob, igconv_dtype_t dtype,
   if (dtype != IGCONV_F16 && dtype != IGCONV_BF16) return IGCONV_ERR_UNSUPPORTED;
   if (dw_dtype != IGCONV_F16 && dw_dtype != IGCONV_BF16 && dw_dtype != IGCONV_F32)
     return IGCONV_ERR_UNSUPPORTED;
+  if (prob->C < 8) return wgrad_few_channels(prob, P, Q, dtype, dw_dtype, X, dY, Cin, dW, alpha,
+                                             beta, workspace, workspace_bytes, stream);
   if ((st = check_limits(prob, P, Q, 8)) != IGCONV_OK) return st;
   if (!aligned16(X) || !aligned16(dY) || !aligned16(dW) || (beta != 0.0f && !aligned16(Cin)) ||
       (workspace && !aligned16(workspace)))

@@ -763,6 +763,45 @@ __global__ void __launch_bounds__(256) filter_taps8_kernel(const uint16_t* __res
   }
 }
 
+// Few-channel dgrad, last step: dst[p][c] = cast(fma(beta, cin[p][c],
+// src8[p][c])) for c < C, from fp32 rows of 8 channels (alpha already
+// applied); the same operations, in the same order, as the GEMM epilogue.
+__global__ void __launch_bounds__(256) unpad_channels_kernel(const float4* __restrict__ src8,
+                                                             uint16_t* __restrict__ dst,
+                                                             long long pixels, int C,
+                                                             int out_bf16,
+                                                             const uint16_t* __restrict__ cin,
+                                                             float beta) {
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < pixels;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const float4 a = src8[2 * i], b = src8[2 * i + 1];
+    const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    for (int c = 0; c < C; ++c) {
+      float x = v[c];
+      if (beta != 0.0f) {
+        const uint16_t u = cin[i * C + c];
+        const float cv = out_bf16 ? __uint_as_float(static_cast<uint32_t>(u) << 16)
+                                  : __half2float(__ushort_as_half(u));
+        x = __fmaf_rn(beta, cv, x);
+      }
+      dst[i * C + c] = out_bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(x))
+                                : __half_as_ushort(__float2half_rn(x));
+    }
+  }
+}
+
+cudaError_t launch_unpad_channels(const float* src8, void* dst, long long pixels, int C,
+                                  int out_bf16, const void* cin, float beta, cudaStream_t s) {
+  if (C < 1 || C > 8) return cudaErrorInvalidValue;
+  long long blocks = (pixels + 255) / 256;
+  if (blocks < 1) blocks = 1;
+  if (blocks > 16384) blocks = 16384;
+  unpad_channels_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+      reinterpret_cast<const float4*>(src8), static_cast<uint16_t*>(dst), pixels, C, out_bf16,
+      static_cast<const uint16_t*>(cin), beta);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_pad_pixels8(const void* src, void* dst, long long pixels, int C,
                                cudaStream_t s) {
   if (C < 1 || C > 8) return cudaErrorInvalidValue;

@@ -405,7 +405,8 @@ __device__ __forceinline__ void issue_stage_loads(const ProdCtx& c, const Produc
     const int q = rem - pp * c.wg_Q;
     const int bh = c.wg_lower_h + pp * c.wg_sh;
     const int bw = c.wg_lower_w + q * c.wg_sw;
-    const bool x_is_a = (c.a_src == SRC_IM2COL_MN);
+    const bool x_is_a = (c.a_src == SRC_IM2COL_MN || c.a_src == SRC_IM2COL_TAPS_MN);
+    const bool x_taps = (c.a_src == SRC_IM2COL_TAPS_MN || c.b_src == SRC_IM2COL_TAPS_MN);
     uint8_t* x_dst = x_is_a ? sA : sB;
     uint8_t* y_dst = x_is_a ? sB : sA;
     constexpr int XA = 2, XB = BN / 64;  // 64-wide chunks per operand tile
@@ -413,7 +414,25 @@ __device__ __forceinline__ void issue_stage_loads(const ProdCtx& c, const Produc
     const int y_chunks = x_is_a ? XB : XA;
     const int x_tile = x_is_a ? s.w.tile_m : s.w.tile_n;
     const int y_tile = x_is_a ? s.w.tile_n : s.w.tile_m;
-    for (int i = 0; i < x_chunks; ++i) {
+    if (x_taps) {
+      // few channels: chunk g holds taps 8g .. 8g + 7 of 8 channels each;
+      // taps past R * S only pad the last chunk (their rows are never
+      // written back), so any valid tap is loaded there
+      for (int i = 0; i < x_chunks; ++i) {
+        const int g = x_tile * x_chunks + i;
+#pragma unroll 1
+        for (int t8 = 0; t8 < 8; ++t8) {
+          int tap = g * 8 + t8;
+          if (tap >= c.wg_RS) tap = c.wg_RS - 1;
+          const int r = tap / c.wg_S;
+          const int sc = tap - r * c.wg_S;
+          tma_load_im2col_4d(x_dst + i * 8192 + t8 * 1024, c.mapA0, bar, 0, bw, bh, n,
+                             static_cast<uint16_t>(sc * c.wg_dw),
+                             static_cast<uint16_t>(r * c.wg_dh));
+        }
+      }
+    }
+    for (int i = 0; i < (x_taps ? 0 : x_chunks); ++i) {
       const int g = x_tile * x_chunks + i;  // 64-wide chunk of the (tap, c) extent
       int tap = g / c.sc.cblocks;
       const int cb = g - tap * c.sc.cblocks;
@@ -573,6 +592,14 @@ __device__ __forceinline__ void run_mma(const ConvGemmParams& p, uint8_t* pipe, 
   const Sched sc = load_sched<PAIR>(p);
   const bool a_mn = (p.a_src == SRC_IM2COL_MN || p.a_src == SRC_2D_MN);
   const bool b_mn = (p.b_src == SRC_W_MN || p.b_src == SRC_IM2COL_MN || p.b_src == SRC_2D_MN);
+  // tap-packed few-channel X side of wgrad: no swizzle, MN-major, 8-channel
+  // groups (one filter tap each) 1 KB apart along MN, 8-position groups 128 B
+  // apart along K; one K = 16 step is 256 bytes.  Without swizzle an MN-major
+  // operand takes its MN-direction stride in the stride-byte-offset field and
+  // its K-direction stride in the leading-byte-offset field (the reverse of
+  // the swizzled MN-major layouts)
+  const bool a_tmn = p.a_src == SRC_IM2COL_TAPS_MN;
+  const bool b_tmn = p.b_src == SRC_IM2COL_TAPS_MN;
   const uint32_t idesc = p.idesc;
   const int num_acc = p.num_acc;
   const int kb_per_acc = p.kb_per_acc;
@@ -584,12 +611,14 @@ __device__ __forceinline__ void run_mma(const ConvGemmParams& p, uint8_t* pipe, 
   // tap-packed operands (few channels) have no swizzle: a region of
   // [rows][16 bytes] per tap, one K = 16 step is two regions
   const bool taps = p.a_src == SRC_IM2COL_TAPS;
-  const uint64_t a0 = taps ? make_smem_desc_noswizzle(pipe_addr, 2048, 128)
-                           : make_smem_desc(pipe_addr, a_mn ? 8192 : 16, 1024);
-  const uint64_t b0 = taps ? make_smem_desc_noswizzle(pipe_addr + C::A_BYTES, BN * 16, 128)
-                           : make_smem_desc(pipe_addr + C::A_BYTES, b_mn ? 8192 : 16, 1024);
-  const uint64_t ak = taps ? 4096 / 16 : (a_mn ? 2048 / 16 : 32 / 16);  // one K = 16 step
-  const uint64_t bk = taps ? 2 * BN * 16 / 16 : (b_mn ? 2048 / 16 : 32 / 16);
+  const uint64_t a0 = taps    ? make_smem_desc_noswizzle(pipe_addr, 2048, 128)
+                      : a_tmn ? make_smem_desc_noswizzle(pipe_addr, 128, 1024)
+                              : make_smem_desc(pipe_addr, a_mn ? 8192 : 16, 1024);
+  const uint64_t b0 = taps    ? make_smem_desc_noswizzle(pipe_addr + C::A_BYTES, BN * 16, 128)
+                      : b_tmn ? make_smem_desc_noswizzle(pipe_addr + C::A_BYTES, 128, 1024)
+                              : make_smem_desc(pipe_addr + C::A_BYTES, b_mn ? 8192 : 16, 1024);
+  const uint64_t ak = taps ? 4096 / 16 : (a_tmn ? 256 / 16 : (a_mn ? 2048 / 16 : 32 / 16));
+  const uint64_t bk = taps ? 2 * BN * 16 / 16 : (b_tmn ? 256 / 16 : (b_mn ? 2048 / 16 : 32 / 16));
   constexpr uint32_t kStageUnits = C::STAGE / 16;
   int stage = 0;        // stage of the first block of the next unit
   uint32_t phase = 0;
@@ -883,6 +912,7 @@ struct EpiCtx {
   int box64;            // 16-bit output boxes of 64 columns (128-byte swizzle)
   int ws_rows_per_split;   // M_pad (wgrad)
   int int_acc;             // accumulators hold exact integers: sum and store them as int32
+  int out_f32;             // write alpha * acc as fp32
   const CUtensorMap* mapY;
 };
 
@@ -917,6 +947,7 @@ __device__ __forceinline__ void run_epilogue(const ConvGemmParams& p, uint64_t* 
   e.box64 = p.use_tma_store && p.store_box64 && e.sc.epi == EPI_STORE;
   e.ws_rows_per_split = p.tiles_m_total * kBlockM;
   e.int_acc = p.int_acc;
+  e.out_f32 = p.out_f32;
   e.mapY = &p.mapY;
   // bias_s holds the whole bias vector when it fits in kBiasBytes (fp32 for
   // the 16-bit passes, int32 for int8); every lane reads the same entries,
@@ -1095,6 +1126,58 @@ __device__ __forceinline__ void run_epilogue(const ConvGemmParams& p, uint64_t* 
         const int n0 = w.tile_n * BN + j * 32;
         if (n0 >= e.N_gemm) break;  // warp-uniform
         const int ncols = min(32, e.N_gemm - n0);
+        if (e.out_f32) {
+          // alpha * (the issuers' accumulators added in the 16-bit path's
+          // order), as fp32: 16 columns (64 bytes) per row store, the last
+          // one cut to the valid columns (a multiple of 4)
+          float v[32];
+          if (has_acc) {
+            uint32_t a0[32];
+            tmem_ld_32x32b_x32(t_row + lone + j * 32, a0);
+            if (use1 && lone == 0u) {
+              uint32_t a1[32];
+              tmem_ld_32x32b_x32(t_row + BN + j * 32, a1);
+              tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                v[i] = __fadd_rn(__uint_as_float(a0[i]), __uint_as_float(a1[i]));
+            } else {
+              tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(a0[i]);
+            }
+            for (int a = 2; a < e.num_acc; ++a) {
+              if (!acc_used(e.kb_per_acc, a, NI, nk, q0)) continue;
+              tmem_ld_32x32b_x32(t_row + a * BN + j * 32, a0);
+              tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = __fadd_rn(v[i], __uint_as_float(a0[i]));
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+          }
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(e.alpha, v[i]);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            if (16 * h >= ncols) break;  // warp-uniform
+            const int n16 = min(4, (ncols - 16 * h) / 4);
+            const uint4 o[4] = {
+                make_uint4(__float_as_uint(v[16 * h]), __float_as_uint(v[16 * h + 1]),
+                           __float_as_uint(v[16 * h + 2]), __float_as_uint(v[16 * h + 3])),
+                make_uint4(__float_as_uint(v[16 * h + 4]), __float_as_uint(v[16 * h + 5]),
+                           __float_as_uint(v[16 * h + 6]), __float_as_uint(v[16 * h + 7])),
+                make_uint4(__float_as_uint(v[16 * h + 8]), __float_as_uint(v[16 * h + 9]),
+                           __float_as_uint(v[16 * h + 10]), __float_as_uint(v[16 * h + 11])),
+                make_uint4(__float_as_uint(v[16 * h + 12]), __float_as_uint(v[16 * h + 13]),
+                           __float_as_uint(v[16 * h + 14]), __float_as_uint(v[16 * h + 15]))};
+            warp_store_rows(stage, o, n16, valid ? row_off * 4 : -1LL,
+                            static_cast<uint8_t*>(e.out) + static_cast<long long>(n0 + 16 * h) * 4,
+                            lane);
+          }
+          continue;
+        }
         if (e.int_acc) {
           // int8 dgrad: the exact int32 sum, written as two 16-column rows
           // of 64 bytes (the column count is a multiple of 16)

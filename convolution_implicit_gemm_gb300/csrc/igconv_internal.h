@@ -33,6 +33,11 @@ enum SrcKind : int {
   // x 64 channels (NDHWC, taps (t, r, s)), K-major; the filter is read as
   // [K][T*R][S][C] (SRC_W_K for fprop, SRC_W_MN with flipped taps for dgrad)
   SRC_IM2COL_K3 = 7,
+  // few channels in wgrad (C <= 8, pixels padded to 8 channels): a 64-row
+  // chunk of the X side is 8 filter taps x 8 channels, eight im2col loads of
+  // 64 positions x 16 bytes stored without swizzle, MN-major: tap t of the
+  // chunk at 1 KB * t, positions at 16 bytes (8-position groups 128 B apart)
+  SRC_IM2COL_TAPS_MN = 8,
 };
 
 enum EpiKind : int {
@@ -127,6 +132,8 @@ struct ConvGemmParams {
                               // 1 one group of eight warps per tile (two buffers)
   int conv_split;             // 1 with EPI_PARTIAL: split-K over a convolution (fprop or
                               // stride-1 dgrad): conv operand loads, fp32 partial tiles
+  int out_f32;                // 1 with EPI_STORE: write alpha * acc as fp32 (no bias, beta
+                              // or cast; a later kernel finishes the output)
   int int_acc;                // 1: the accumulators hold exact integers (int8 operands on the
                               // fp16 path); EPI_STORE writes their int32 sum, EPI_PARTIAL
                               // int32 partial sums (int8 dgrad / wgrad)
@@ -151,6 +158,8 @@ cudaError_t launch_conv_splitk_reduce(const float* ws, int splits, long long spl
                                       int ws_ld, long long rows, int cols, void* out,
                                       int out_bf16, const void* cin, const void* bias,
                                       float alpha, float beta, int relu, cudaStream_t s);
+cudaError_t launch_unpad_channels(const float* src8, void* dst, long long pixels, int C,
+                                  int out_bf16, const void* cin, float beta, cudaStream_t s);
 cudaError_t launch_wgrad_reduce_i32(const int* ws, int splits, long long split_stride, int ws_ld,
                                     int rows, int cols, int swapped, int K, int RS, int C,
                                     int cpad, int* dW, cudaStream_t s);

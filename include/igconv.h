@@ -166,7 +166,8 @@ IGCONV_API igconv_status_t conv2d_fprop_ws(const igconv_problem_t *prob, igconv_
  *   dtype    IGCONV_F16 or IGCONV_BF16 for dY, Wt, Cin, dX.
  *   dY [N][P][Q][K]   Wt [K][R][S][C]   dX [N][H][W][C] (written, every element)
  *   Cin [N][H][W][C], read only when beta != 0.
- * Errors: as conv2d_fprop; also UNSUPPORTED when stride_h*stride_w > 16. */
+ * Errors: as conv2d_fprop; also UNSUPPORTED when stride_h*stride_w > 16;
+ * WORKSPACE when C < 8 (that path needs conv2d_dgrad_ws). */
 IGCONV_API igconv_status_t conv2d_dgrad(const igconv_problem_t *prob, igconv_dtype_t dtype,
                                         const void *dY, const void *Wt, const void *Cin,
                                         void *dX, float alpha, float beta, void *stream);
@@ -176,9 +177,15 @@ IGCONV_API igconv_status_t conv2d_dgrad(const igconv_problem_t *prob, igconv_dty
  * workspace, an ordered reduction applying alpha and beta * Cin) when the
  * tuning knob IGCONV_TUNE_CONV_SPLITS asks for it.  The size query returns 0
  * (no workspace needed) for strided problems and unsplit plans, which by
- * default is every plan; it is host-only and queried on the current device.  Arguments, errors and the
- * result definition as conv2d_dgrad; WORKSPACE when a split plan's
- * workspace is too small. */
+ * default is every plan; it is host-only and queried on the current device.
+ * Few input channels (C < 8, the first layer of a CNN): the data gradient
+ * runs over the filter copied to 8 channels per tap, writes alpha * acc as
+ * fp32 rows of 8 channels, and a second kernel adds beta * Cin to the C real
+ * channels and casts.  Both copies live in the workspace, so C < 8 always
+ * needs one (round256(K*R*S*16) + round256(N*H*W*32) bytes, from the size
+ * query); dY must be 16-byte aligned, Wt, dX and Cin only 2-byte aligned.
+ * Arguments, errors and the result definition as conv2d_dgrad; WORKSPACE
+ * when a split or few-channel plan's workspace is missing or too small. */
 IGCONV_API size_t conv2d_dgrad_workspace_size(const igconv_problem_t *prob,
                                               igconv_dtype_t dtype);
 IGCONV_API igconv_status_t conv2d_dgrad_ws(const igconv_problem_t *prob, igconv_dtype_t dtype,
@@ -187,7 +194,8 @@ IGCONV_API igconv_status_t conv2d_dgrad_ws(const igconv_problem_t *prob, igconv_
                                            size_t workspace_bytes, void *stream);
 
 /* Bytes of device workspace conv2d_wgrad needs for this problem (fp32
- * split-K partial sums).  The split count depends on the SM count of the
+ * split-K partial sums; for C < 8 also the pixels copied to 8-channel rows,
+ * round256(N*H*W*16) bytes, ahead of the partials).  The split count depends on the SM count of the
  * current device, which this call queries (no work is enqueued); call it
  * with the same device current as the conv2d_wgrad call.  Returns 0 for an
  * invalid problem. */
@@ -202,6 +210,11 @@ IGCONV_API size_t conv2d_wgrad_workspace_size(const igconv_problem_t *prob,
  * kernel); apache/tvm PR #10177 (fp32 accumulation; GEMM-K is N*P*Q, so
  * split-K is needed).  The partial sums are added in a fixed order, so the
  * result is bit-identical from run to run.
+ * Few input channels (C < 8): the pixels are copied to 8-channel rows in the
+ * workspace and each 64-row reduction operand packs 8 filter taps x 8
+ * channels, so a 7x7 filter takes 7 operand row blocks instead of 49; the
+ * reduction writes the C real channels.  X then needs only 2-byte alignment
+ * and dW / Cin only their element size; dY stays 16-byte aligned.
  *   dtype     IGCONV_F16 or IGCONV_BF16 for X and dY.
  *   dw_dtype  IGCONV_F16, IGCONV_BF16 or IGCONV_F32 for dW and Cin.
  *   X [N][H][W][C]   dY [N][P][Q][K]   dW [K][R][S][C] (written)
