@@ -719,13 +719,16 @@ def measure_rows(args, device, stream):
             r[kind] = {"TFLOP/s": L.flops / (ms * 1e-3) / 1e12, "ms": ms}
         rows[name] = r
         del L
-    # the first layer of a CNN (3 input channels): the few-channel fprop
-    # path, its pixel and filter copies included in the time
+    # the first layer of a CNN (3 input channels): the few-channel paths,
+    # their 8-channel copies included in the time
     L = Layer("resnet50_stem_224x224_3to64_7x7_s2", device=device)
-    ms = time_call(L.fprop, stream, flush=flush)
-    rows["resnet50_stem_224x224_3to64_7x7_s2"] = {
-        "fprop": {"TFLOP/s": L.flops / (ms * 1e-3) / 1e12, "ms": ms,
-                  "includes": "8-channel pixel and filter copies + GEMM"}}
+    r = {}
+    for kind, what in (("fprop", "8-channel pixel and filter copies + GEMM"),
+                       ("dgrad", "8-channel filter copy + GEMM to fp32 rows + unpad/cast"),
+                       ("wgrad", "8-channel pixel copy + tap-packed GEMM + split reduction")):
+        ms = time_call(getattr(L, kind), stream, flush=flush)
+        r[kind] = {"TFLOP/s": L.flops / (ms * 1e-3) / 1e12, "ms": ms, "includes": what}
+    rows["resnet50_stem_224x224_3to64_7x7_s2"] = r
     del L
     rows.update(measure_depthwise_rows(device, stream, flush))
     # 3D forward convolution (5D im2col implicit GEMM)

@@ -46,7 +46,7 @@ DeviceState g_dev[kMaxDevices];
 PFN_encodeTiled g_encode_tiled = nullptr;
 PFN_encodeIm2col g_encode_im2col = nullptr;
 std::atomic<int> g_tune_splits{0}, g_tune_bn{0}, g_tune_max_ctas{0}, g_tune_no_pairs{0},
-    g_tune_epi_groups{0}, g_tune_conv_splits{0};
+    g_tune_epi_groups{0}, g_tune_conv_splits{0}, g_tune_few_channels{0};
 
 igconv_status_t device_state(DeviceState** out) {
   int dev = 0;
@@ -138,15 +138,23 @@ CUtensorMapDataType tma_dtype(int bf16) {
 // positions x 64 channels per load, 128-byte swizzle.  The box corners and
 // traversal strides describe the grid of filter-origin positions: the
 // traversal visits lower .. (extent - 1 + upper) in steps of trav.
+// x_strides (bytes between pixels, rows and images) replaces the dense NHWC
+// strides when given: the few-channel packed image is read with a pixel
+// stride smaller than the 64-channel box, so consecutive boxes overlap.
 bool encode_im2col(CUtensorMap* map, const void* base, int bf16, int n, int h, int w, int c,
                    int lower_h, int lower_w, int upper_h, int upper_w, int trav_h, int trav_w,
                    int pixels, int channels_box = 64,
-                   CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+                   CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B,
+                   const cuuint64_t* x_strides = nullptr) {
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(c), static_cast<cuuint64_t>(w),
                               static_cast<cuuint64_t>(h), static_cast<cuuint64_t>(n)};
-  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(c) * 2,
-                                 static_cast<cuuint64_t>(c) * 2 * w,
-                                 static_cast<cuuint64_t>(c) * 2 * w * h};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(c) * 2, static_cast<cuuint64_t>(c) * 2 * w,
+                           static_cast<cuuint64_t>(c) * 2 * w * h};
+  if (x_strides) {
+    strides[0] = x_strides[0];
+    strides[1] = x_strides[1];
+    strides[2] = x_strides[2];
+  }
   const int lower[2] = {lower_w, lower_h};
   const int upper[2] = {upper_w, upper_h};
   const cuuint32_t estr[4] = {1, static_cast<cuuint32_t>(trav_w), static_cast<cuuint32_t>(trav_h),
@@ -318,7 +326,8 @@ void init_common(ConvGemmParams& p, const DeviceState* st) {
 // fprop plan (16-bit, or the int8 path's widened copies) on X [N,H,W,C],
 // Wt [K,R,S,C], tile width bn.
 igconv_status_t plan_fprop(ConvGemmParams& p, int bn, const igconv_problem_t* pb, int P, int Q,
-                           int bf16, const void* X, const void* Wt) {
+                           int bf16, const void* X, const void* Wt,
+                           const cuuint64_t* x_strides = nullptr) {
   if (bn != 64 && bn != 128 && bn != 256) return IGCONV_ERR_INVALID_ARG;
   const long long M = static_cast<long long>(pb->N) * P * Q;
   SubProblem& sp = p.sub[0];
@@ -349,7 +358,8 @@ igconv_status_t plan_fprop(ConvGemmParams& p, int bn, const igconv_problem_t* pb
   // box of filter-origin positions: [-pad, H - 1 + pad - dil*(R-1)]
   if (!encode_im2col(&p.mapA[0], X, bf16, pb->N, pb->H, pb->W, pb->C, -pb->pad_h, -pb->pad_w,
                      pb->pad_h - (pb->R - 1) * pb->dil_h, pb->pad_w - (pb->S - 1) * pb->dil_w,
-                     pb->stride_h, pb->stride_w, kBlockM))
+                     pb->stride_h, pb->stride_w, kBlockM, 64, CU_TENSOR_MAP_SWIZZLE_128B,
+                     x_strides))
     return IGCONV_ERR_UNSUPPORTED;
   p.mapA_valid = 1u;
   if (!encode_filter(&p.mapB, Wt, bf16, pb->K, pb->R, pb->S, pb->C, bn))
@@ -372,6 +382,72 @@ FewChannelWs few_channel_ws(const igconv_problem_t* pb) {
   w.w_bytes = round256(static_cast<size_t>(ceil_div(pb->R * pb->S, 8)) *
                        static_cast<size_t>(ceil_div(pb->K, 256)) * 256 * 128);
   w.total = w.x_bytes + w.w_bytes;
+  return w;
+}
+
+int floor_div(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
+
+// Few-channel packing (FewPack, igconv_internal.h) for C <= 8 at dilation 1
+// with fh * fw * C <= 64 (fh, fw the strides): the stem's 7x7 stride-2
+// filter over 3 channels becomes a stride-1 4x4 one over 2x2x3 (padded to
+// 16) channels, four packed pixels per 128-byte row: 4 reduction blocks of
+// 64 instead of 7 of the tap-packed path, each one full-width TMA load
+// instead of eight 16-byte ones.  Off when IGCONV_TUNE_FEW_CHANNELS is 1.
+bool few_pack_plan(const igconv_problem_t* pb, int P, int Q, FewPack* f) {
+  if (g_tune_few_channels.load() == 1) return false;
+  if (pb->C > 8 || pb->dil_h != 1 || pb->dil_w != 1) return false;
+  const int z = pb->stride_h * pb->stride_w * pb->C;
+  if (z > 64) return false;
+  f->fh = pb->stride_h;
+  f->fw = pb->stride_w;
+  f->C = pb->C;
+  f->R = pb->R;
+  f->S = pb->S;
+  f->ph = pb->pad_h;
+  f->pw = pb->pad_w;
+  f->cz = 8;
+  while (f->cz < z) f->cz *= 2;
+  f->ppr = 64 / f->cz;
+  f->A0 = floor_div(-pb->pad_h, f->fh);
+  f->B0 = floor_div(-pb->pad_w, f->fw);
+  f->R2 = floor_div(pb->R - 1 - pb->pad_h, f->fh) - f->A0 + 1;
+  const int S2 = floor_div(pb->S - 1 - pb->pad_w, f->fw) - f->B0 + 1;
+  f->Sv = ceil_div(S2, f->ppr);
+  f->Hz = P + f->R2 - 1;
+  f->Wv = Q + (f->Sv - 1) * f->ppr;
+  f->Wz = f->Wv + f->ppr - 1;
+  const long long row_bytes = static_cast<long long>(f->Wz) * f->cz * 2;
+  return row_bytes * f->Hz * pb->N < (1LL << 40) && f->Hz < (1 << 24) && f->Wz < (1 << 24);
+}
+
+// The stride-1 problem the packed image and filter define: 64 channels,
+// R2 x Sv taps (Sv along w, ppr packed pixels apart), no padding.
+igconv_problem_t few_pack_problem(const igconv_problem_t* pb, const FewPack& f) {
+  igconv_problem_t v = *pb;
+  v.H = f.Hz;
+  v.W = f.Wv;
+  v.C = 64;
+  v.R = f.R2;
+  v.S = f.Sv;
+  v.pad_h = v.pad_w = 0;
+  v.stride_h = v.stride_w = 1;
+  v.dil_h = 1;
+  v.dil_w = f.ppr;
+  return v;
+}
+
+struct FewPackWs {
+  size_t z_bytes, w_bytes;
+  cuuint64_t strides[3];  // pixel, row, image strides of the packed image
+};
+FewPackWs few_pack_ws(const igconv_problem_t* pb, const FewPack& f) {
+  FewPackWs w;
+  const cuuint64_t px = static_cast<cuuint64_t>(f.cz) * 2;
+  w.strides[0] = px;
+  w.strides[1] = px * f.Wz;
+  w.strides[2] = px * f.Wz * f.Hz;
+  w.z_bytes = round256(static_cast<size_t>(w.strides[2]) * pb->N);
+  w.w_bytes = round256(static_cast<size_t>(pb->K) * f.R2 * f.Sv * 128);
   return w;
 }
 
@@ -1092,6 +1168,66 @@ bool wino_shape(const igconv_problem_t* pb) {
          pb->dil_w == 1;
 }
 
+
+// The wgrad GEMM over geometry g (the problem itself, or the few-channel
+// packed one, whose X map then has the strides x_strides) into the split
+// partials `part`, then the ordered reduction into dW [K][RS][C] of the real
+// problem, workspace rows decoded by remap when given.
+igconv_status_t run_wgrad(const igconv_problem_t* g, int P, int Q, const WgradPlan& w, int bf16,
+                          const void* X, const cuuint64_t* x_strides, const void* dY, void* part,
+                          const DeviceState* dev, int RS, int C, const FewPack* remap, void* dW,
+                          igconv_dtype_t dw_dtype, const void* Cin, float alpha, float beta,
+                          cudaStream_t s) {
+  ConvGemmParams p;
+  init_common(p, dev);
+  p.nsub = 1;
+  p.a_src = w.swapped ? SRC_2D_MN : SRC_IM2COL_MN;
+  p.b_src = w.swapped ? SRC_IM2COL_MN : SRC_2D_MN;
+  p.epi = EPI_PARTIAL;
+  p.tiles_m_total = w.tiles_m;
+  p.tiles_n = w.tiles_n;
+  p.splits = w.splits;
+  p.kblocks_total = w.kblocks;
+  p.units = w.tiles_m * w.tiles_n * w.splits;
+  p.cblocks = w.cblocks;
+  p.N_gemm = w.N_pad;
+  p.idesc = make_idesc(kBlockM, w.bn, bf16, 1, 1);
+  set_fp_accumulators(p, w.bn);
+  p.wg_PQ = P * Q;
+  p.wg_Q = Q;
+  p.wg_lower_h = -g->pad_h;
+  p.wg_lower_w = -g->pad_w;
+  p.wg_sh = g->stride_h;
+  p.wg_sw = g->stride_w;
+  p.wg_S = g->S;
+  p.wg_RS = w.rs;
+  p.wg_dh = g->dil_h;
+  p.wg_dw = g->dil_w;
+  p.wg_K = g->K;
+  p.out = part;
+  p.ws_split_stride = static_cast<long long>(w.M_pad) * w.N_pad;
+  p.ws_ld = w.N_pad;
+  p.use_tma_store = encode_out_2d(&p.mapY, part, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
+                                  static_cast<long long>(w.splits) * w.M_pad, w.N_pad, 16,
+                                  CU_TENSOR_MAP_SWIZZLE_64B) ? 1 : 0;
+  if (!encode_im2col(&p.mapA[0], X, bf16, g->N, g->H, g->W, g->C, -g->pad_h, -g->pad_w,
+                     g->pad_h - (g->R - 1) * g->dil_h, g->pad_w - (g->S - 1) * g->dil_w,
+                     g->stride_h, g->stride_w, kBlockK, 64, CU_TENSOR_MAP_SWIZZLE_128B,
+                     x_strides))
+    return IGCONV_ERR_UNSUPPORTED;
+  p.mapA_valid = 1u;
+  const long long npq = static_cast<long long>(g->N) * P * Q;
+  if (!encode_2d(&p.mapB, dY, bf16, npq, g->K)) return IGCONV_ERR_UNSUPPORTED;
+  if (launch_conv_gemm(p, w.bn, grid_for(p.units, dev), s) != cudaSuccess) return IGCONV_ERR_CUDA;
+  const int dwt = dw_dtype == IGCONV_F32 ? 2 : (dw_dtype == IGCONV_BF16 ? 1 : 0);
+  const int xext = w.rs * w.cpad;
+  return from_cuda(launch_wgrad_reduce(static_cast<const float*>(part), w.splits,
+                                       p.ws_split_stride, w.N_pad, w.swapped ? g->K : xext,
+                                       w.swapped ? xext : g->K, w.swapped, g->K, RS, C, w.cpad,
+                                       dW, dwt, beta != 0.0f ? Cin : nullptr, alpha, beta, s,
+                                       remap));
+}
+
 }  // namespace
 
 extern "C" {
@@ -1140,6 +1276,10 @@ igconv_status_t igconv_set_tuning(igconv_tune_key_t key, int value) {
       if (value < 0 || value > 16) return IGCONV_ERR_INVALID_ARG;
       g_tune_conv_splits.store(value);
       return IGCONV_OK;
+    case IGCONV_TUNE_FEW_CHANNELS:
+      if (value < 0 || value > 1) return IGCONV_ERR_INVALID_ARG;
+      g_tune_few_channels.store(value);
+      return IGCONV_OK;
   }
   return IGCONV_ERR_INVALID_ARG;
 }
@@ -1148,7 +1288,14 @@ size_t conv2d_fprop_workspace_size(const igconv_problem_t* prob, igconv_dtype_t 
   int P = 0, Q = 0;
   if (check_shape(prob, &P, &Q) != IGCONV_OK) return 0;
   if (dtype != IGCONV_F16 && dtype != IGCONV_BF16) return 0;
-  if (prob->C <= 8) return few_channel_ws(prob).total;
+  if (prob->C <= 8) {
+    FewPack f;
+    if (few_pack_plan(prob, P, Q, &f)) {
+      const FewPackWs pw = few_pack_ws(prob, f);
+      return pw.z_bytes + pw.w_bytes;
+    }
+    return few_channel_ws(prob).total;
+  }
   // split-K partials, when the plan splits (the same decision as conv2d_fprop_ws)
   const int sms = current_sm_count();
   const long long tiles_m = ceil_div(static_cast<long long>(prob->N) * P * Q, kBlockM);
@@ -1178,14 +1325,19 @@ igconv_status_t conv2d_fprop_ws(const igconv_problem_t* prob, igconv_dtype_t dty
   if (!X || !Wt || !Y || (beta != 0.0f && !Cin)) return IGCONV_ERR_INVALID_ARG;
   if (!std::isfinite(alpha) || !std::isfinite(beta)) return IGCONV_ERR_INVALID_ARG;
   if (dtype != IGCONV_F16 && dtype != IGCONV_BF16) return IGCONV_ERR_UNSUPPORTED;
-  // few channels: C < 8 always, C == 8 when a workspace is given
+  // few channels: C < 8 always, C == 8 when a workspace is given; packed
+  // (space-to-depth, FewPack) where few_pack_plan allows, else tap-packed
   const bool few = prob->C < 8 || (prob->C == 8 && workspace != nullptr);
+  FewPack fpk{};
+  const bool packed = few && few_pack_plan(prob, P, Q, &fpk);
+  igconv_problem_t vp = packed ? few_pack_problem(prob, fpk) : *prob;
   if (few) {
     igconv_problem_t k8 = *prob;
     k8.C = 8;  // the limits apply to the padded pixels; K must still be a multiple of 8
-    if ((st = check_limits(&k8, P, Q, 8)) != IGCONV_OK) return st;
-    const FewChannelWs fw = few_channel_ws(prob);
-    if (!workspace || workspace_bytes < fw.total) return IGCONV_ERR_WORKSPACE;
+    if ((st = check_limits(packed ? &vp : &k8, P, Q, 8)) != IGCONV_OK) return st;
+    const size_t need = packed ? few_pack_ws(prob, fpk).z_bytes + few_pack_ws(prob, fpk).w_bytes
+                               : few_channel_ws(prob).total;
+    if (!workspace || workspace_bytes < need) return IGCONV_ERR_WORKSPACE;
     if (!aligned16(workspace) || !aligned16(Y) || (bias && !aligned16(bias)) ||
         (beta != 0.0f && !aligned16(Cin)) || (prob->C == 8 && !aligned16(X)) ||
         (reinterpret_cast<uintptr_t>(X) & 1) || (reinterpret_cast<uintptr_t>(Wt) & 1))
@@ -1204,7 +1356,18 @@ igconv_status_t conv2d_fprop_ws(const igconv_problem_t* prob, igconv_dtype_t dty
   const int bn = choose_block_n(prob->K, ceil_div(static_cast<long long>(prob->N) * P * Q, kBlockM),
                                 dev->sm_count);
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  if (few) {
+  const void* gW = Wt;  // the filter the GEMM reads
+  if (packed) {
+    const FewPackWs pw = few_pack_ws(prob, fpk);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    void* Zp = ws;
+    void* Wpk = ws + pw.z_bytes;
+    if (launch_few_pack_x(X, Zp, fpk, prob->N, prob->H, prob->W, cs) != cudaSuccess ||
+        launch_few_pack_filter(Wt, Wpk, fpk, prob->K, cs) != cudaSuccess)
+      return IGCONV_ERR_CUDA;
+    if ((st = plan_fprop(p, bn, &vp, P, Q, bf16, Zp, Wpk, pw.strides)) != IGCONV_OK) return st;
+    gW = Wpk;
+  } else if (few) {
     const FewChannelWs fw = few_channel_ws(prob);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     const void* X8 = X;
@@ -1228,12 +1391,12 @@ igconv_status_t conv2d_fprop_ws(const igconv_problem_t* prob, igconv_dtype_t dty
                               p.sub[0].rcount * p.sub[0].scount * p.cblocks, dev->sm_count);
     if (splits > 1 && workspace_bytes < conv_split_bytes(p, bn, splits)) return IGCONV_ERR_WORKSPACE;
   }
-  if (!few && splits == 1 && use_pairs(bn, p.sub[0].tiles_m, false)) {
+  if ((!few || packed) && splits == 1 && use_pairs(bn, p.sub[0].tiles_m, false)) {
     // 256-row units; each CTA of a pair loads bn/2 filter rows
     p.pair = 1;
     p.units = ceil_div(p.sub[0].tiles_m, 2) * p.tiles_n;
     p.idesc = make_idesc(2 * kBlockM, bn, bf16, 0, 0);
-    if (!encode_filter(&p.mapB, Wt, bf16, prob->K, prob->R, prob->S, prob->C, bn / 2))
+    if (!encode_filter(&p.mapB, gW, bf16, vp.K, vp.R, vp.S, vp.C, bn / 2))
       return IGCONV_ERR_UNSUPPORTED;
   }
   p.epi = EPI_STORE;
@@ -1423,7 +1586,14 @@ size_t conv2d_wgrad_workspace_size(const igconv_problem_t* prob, igconv_dtype_t 
     cudaGetLastError();  // no device: size for the default SM count
   }
   WgradPlan w;
-  if (prob->C < 8) {  // few channels: the 8-channel pixel copy, then the partials
+  if (prob->C < 8) {
+    FewPack f;
+    if (few_pack_plan(prob, P, Q, &f)) {  // the packed image, then the partials
+      const igconv_problem_t vp = few_pack_problem(prob, f);
+      plan_wgrad_shape(&vp, P, Q, sm_count, &w);
+      return few_pack_ws(prob, f).z_bytes + w.ws_bytes;
+    }
+    // the 8-channel pixel copy, then the partials
     plan_wgrad_taps(prob, P, Q, sm_count, &w);
     return round256(static_cast<size_t>(prob->N) * prob->H * prob->W * 16) + w.ws_bytes;
   }
@@ -1443,6 +1613,32 @@ igconv_status_t conv2d_wgrad(const igconv_problem_t* prob, igconv_dtype_t dtype,
   if (dtype != IGCONV_F16 && dtype != IGCONV_BF16) return IGCONV_ERR_UNSUPPORTED;
   if (dw_dtype != IGCONV_F16 && dw_dtype != IGCONV_BF16 && dw_dtype != IGCONV_F32)
     return IGCONV_ERR_UNSUPPORTED;
+  const int bf16 = dtype == IGCONV_BF16 ? 1 : 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  FewPack fpk{};
+  if (prob->C < 8 && few_pack_plan(prob, P, Q, &fpk)) {
+    // few channels, packed: the space-to-depth image, then the dense wgrad
+    // of the packed problem, its rows decoded back to (tap, c)
+    const igconv_problem_t vp = few_pack_problem(prob, fpk);
+    if ((st = check_limits(&vp, P, Q, 8)) != IGCONV_OK) return st;
+    const uintptr_t esz = dw_dtype == IGCONV_F32 ? 4 : 2;
+    if ((reinterpret_cast<uintptr_t>(X) & 1) || !aligned16(dY) ||
+        (reinterpret_cast<uintptr_t>(dW) & (esz - 1)) ||
+        (beta != 0.0f && (reinterpret_cast<uintptr_t>(Cin) & (esz - 1))) ||
+        (workspace && !aligned16(workspace)))
+      return IGCONV_ERR_MISALIGNED;
+    DeviceState* dev = nullptr;
+    if ((st = device_state(&dev)) != IGCONV_OK) return st;
+    WgradPlan w;
+    plan_wgrad_shape(&vp, P, Q, dev->sm_count, &w);
+    const FewPackWs pw = few_pack_ws(prob, fpk);
+    if (!workspace || workspace_bytes < pw.z_bytes + w.ws_bytes) return IGCONV_ERR_WORKSPACE;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    if (launch_few_pack_x(X, ws, fpk, prob->N, prob->H, prob->W, s) != cudaSuccess)
+      return IGCONV_ERR_CUDA;
+    return run_wgrad(&vp, P, Q, w, bf16, ws, pw.strides, dY, ws + pw.z_bytes, dev,
+                     prob->R * prob->S, prob->C, &fpk, dW, dw_dtype, Cin, alpha, beta, s);
+  }
   if (prob->C < 8) return wgrad_few_channels(prob, P, Q, dtype, dw_dtype, X, dY, Cin, dW, alpha,
                                              beta, workspace, workspace_bytes, stream);
   if ((st = check_limits(prob, P, Q, 8)) != IGCONV_OK) return st;
@@ -1454,57 +1650,8 @@ igconv_status_t conv2d_wgrad(const igconv_problem_t* prob, igconv_dtype_t dtype,
   WgradPlan w;
   plan_wgrad_shape(prob, P, Q, dev->sm_count, &w);
   if (!workspace || workspace_bytes < w.ws_bytes) return IGCONV_ERR_WORKSPACE;
-  const int bf16 = dtype == IGCONV_BF16 ? 1 : 0;
-  ConvGemmParams p;
-  init_common(p, dev);
-  p.nsub = 1;
-  p.a_src = w.swapped ? SRC_2D_MN : SRC_IM2COL_MN;
-  p.b_src = w.swapped ? SRC_IM2COL_MN : SRC_2D_MN;
-  p.epi = EPI_PARTIAL;
-  p.tiles_m_total = w.tiles_m;
-  p.tiles_n = w.tiles_n;
-  p.splits = w.splits;
-  p.kblocks_total = w.kblocks;
-  p.units = w.tiles_m * w.tiles_n * w.splits;
-  p.cblocks = w.cblocks;
-  p.N_gemm = w.N_pad;
-  p.idesc = make_idesc(kBlockM, w.bn, bf16, 1, 1);
-  set_fp_accumulators(p, w.bn);
-  p.wg_PQ = P * Q;
-  p.wg_Q = Q;
-  p.wg_lower_h = -prob->pad_h;
-  p.wg_lower_w = -prob->pad_w;
-  p.wg_sh = prob->stride_h;
-  p.wg_sw = prob->stride_w;
-  p.wg_S = prob->S;
-  p.wg_RS = w.rs;
-  p.wg_dh = prob->dil_h;
-  p.wg_dw = prob->dil_w;
-  p.wg_K = prob->K;
-  p.out = workspace;
-  p.ws_split_stride = static_cast<long long>(w.M_pad) * w.N_pad;
-  p.ws_ld = w.N_pad;
-  p.use_tma_store = encode_out_2d(&p.mapY, workspace, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
-                                  static_cast<long long>(w.splits) * w.M_pad, w.N_pad, 16,
-                                  CU_TENSOR_MAP_SWIZZLE_64B) ? 1 : 0;
-  if (!encode_im2col(&p.mapA[0], X, bf16, prob->N, prob->H, prob->W, prob->C, -prob->pad_h,
-                     -prob->pad_w, prob->pad_h - (prob->R - 1) * prob->dil_h,
-                     prob->pad_w - (prob->S - 1) * prob->dil_w, prob->stride_h, prob->stride_w,
-                     kBlockK))
-    return IGCONV_ERR_UNSUPPORTED;
-  p.mapA_valid = 1u;
-  const long long npq = static_cast<long long>(prob->N) * P * Q;
-  if (!encode_2d(&p.mapB, dY, bf16, npq, prob->K)) return IGCONV_ERR_UNSUPPORTED;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_conv_gemm(p, w.bn, grid_for(p.units, dev), s);
-  if (e != cudaSuccess) return IGCONV_ERR_CUDA;
-  const int dwt = dw_dtype == IGCONV_F32 ? 2 : (dw_dtype == IGCONV_BF16 ? 1 : 0);
-  const int xext = w.rs * w.cpad;
-  e = launch_wgrad_reduce(static_cast<const float*>(workspace), w.splits, p.ws_split_stride,
-                          w.N_pad, w.swapped ? prob->K : xext, w.swapped ? xext : prob->K,
-                          w.swapped, prob->K, w.rs, prob->C, w.cpad, dW, dwt,
-                          beta != 0.0f ? Cin : nullptr, alpha, beta, s);
-  return from_cuda(e);
+  return run_wgrad(prob, P, Q, w, bf16, X, nullptr, dY, workspace, dev, w.rs, prob->C, nullptr,
+                   dW, dw_dtype, Cin, alpha, beta, s);
 }
 
 // ---------------------------------------------------------------------------

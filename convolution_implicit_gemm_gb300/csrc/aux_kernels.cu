@@ -268,6 +268,16 @@ __device__ __forceinline__ void store4_any(void* p, long long dst, int dtype, fl
   }
 }
 
+// Target (tap, c) of workspace row / column mx: (mx / cpad, mx % cpad), or
+// the few-channel virtual row decode when remap.cz != 0.
+__device__ __forceinline__ bool row_target(int mx, int RS, int C, int cpad, const FewPack& remap,
+                                           int* tap, int* c) {
+  if (remap.cz != 0) return few_pack_decode(remap, mx >> 6, mx & 63, tap, c);
+  *tap = mx / cpad;
+  *c = mx - *tap * cpad;
+  return *tap < RS && *c < C;
+}
+
 // Many splits (more than 8): each warp covers 8 rows x 64 columns with
 // 4-byte loads, so a block holds only 8 rows and the small outputs these
 // plans have still spread over enough blocks; split group g adds splits
@@ -276,7 +286,7 @@ template <int G>
 __global__ void __launch_bounds__(256) wgrad_reduce_many_kernel(
     const float* __restrict__ ws, int splits, long long split_stride, int ws_ld, int rows,
     int cols, int swapped, int K, int RS, int C, int cpad, void* dW, int dw_dtype,
-    const void* cin, float alpha, float beta) {
+    const void* cin, float alpha, float beta, FewPack remap) {
   constexpr int RG = 8 / G;    // row groups
   constexpr int TR = 8 * RG;   // workspace rows per tile
   __shared__ float part[G][TR][65];
@@ -337,9 +347,8 @@ __global__ void __launch_bounds__(256) wgrad_reduce_many_kernel(
       for (int j = 1; j < G; ++j) v = __fadd_rn(v, part[j][rr][cc]);
       const int k = swapped ? r : col;
       const int mx = swapped ? col : r;
-      const int tap = mx / cpad;
-      const int c = mx - tap * cpad;
-      if (k >= K || tap >= RS || c >= C) continue;
+      int tap, c;
+      if (k >= K || !row_target(mx, RS, C, cpad, remap, &tap, &c)) continue;
       const long long dst = (static_cast<long long>(k) * RS + tap) * C + c;  // KRSC
       float o = __fmul_rn(alpha, v);
       if (beta != 0.0f) o = __fmaf_rn(beta, load_any(cin, dst, dw_dtype), o);
@@ -353,7 +362,7 @@ template <int G, bool SWAPPED>
 __global__ void __launch_bounds__(256) wgrad_reduce_kernel(
     const float* __restrict__ ws, int splits, long long split_stride, int ws_ld, int rows,
     int cols, int K, int RS, int C, int cpad, void* dW, int dw_dtype, const void* cin,
-    float alpha, float beta) {
+    float alpha, float beta, FewPack remap) {
   constexpr int RW = 8 / G;   // row warps per split group
   constexpr int RPW = 8;      // rows per warp
   constexpr int TR = RPW * RW;  // workspace rows per tile
@@ -409,7 +418,28 @@ __global__ void __launch_bounds__(256) wgrad_reduce_kernel(
       d[3] = acc[i].w;
     }
     __syncthreads();
-    if (SWAPPED) {
+    if (SWAPPED && remap.cz != 0) {
+      // rows k, few-channel virtual columns: each column decoded on its own
+      const int q = lane;
+      const int cc = c0 + 4 * q;
+      for (int rr = warp; rr < TR; rr += 8) {
+        const int k = r0 + rr;
+        if (k >= rows || k >= K) break;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          int tap, c;
+          if (cc + j >= cols || !few_pack_decode(remap, (cc + j) >> 6, (cc + j) & 63, &tap, &c))
+            continue;
+          float a = part[0][rr][4 * q + j];
+#pragma unroll
+          for (int h = 1; h < G; ++h) a = __fadd_rn(a, part[h][rr][4 * q + j]);
+          float o = __fmul_rn(alpha, a);
+          const long long dst = (static_cast<long long>(k) * RS + tap) * C + c;
+          if (beta != 0.0f) o = __fmaf_rn(beta, load_any(cin, dst, dw_dtype), o);
+          store_any(dW, dst, dw_dtype, o);
+        }
+      }
+    } else if (SWAPPED) {
       // rows k, columns (tap, c): lane q's 4 columns are 4 consecutive c
       const int q = lane;
       const int cc = c0 + 4 * q;
@@ -453,9 +483,8 @@ __global__ void __launch_bounds__(256) wgrad_reduce_kernel(
       const int rr = t % TR;
       const int kq = t / TR;
       const int r = r0 + rr;
-      const int tap = r / cpad;
-      const int c = r - tap * cpad;
-      if (r < rows && tap < RS && c < C) {
+      int tap = 0, c = 0;
+      if (r < rows && row_target(r, RS, C, cpad, remap, &tap, &c)) {
         const long long kstride = static_cast<long long>(RS) * C;
         long long dst = (static_cast<long long>(c0 + kq * KPT) * RS + tap) * C + c;
         for (int j = 0; j < KPT; ++j, dst += kstride) {
@@ -478,14 +507,16 @@ __global__ void __launch_bounds__(256) wgrad_reduce_kernel(
 cudaError_t launch_wgrad_reduce(const float* ws, int splits, long long split_stride, int ws_ld,
                                 int rows, int cols, int swapped, int K, int RS, int C, int cpad,
                                 void* dW, int dw_dtype, const void* cin, float alpha, float beta,
-                                cudaStream_t s) {
+                                cudaStream_t s, const FewPack* remap_in) {
+  FewPack remap{};
+  if (remap_in) remap = *remap_in;  // remap.cz == 0: plain (tap, c) rows
   if (splits > 8) {
     constexpr int TR = 8;
     const long long tiles = static_cast<long long>((rows + TR - 1) / TR) * ((cols + 63) / 64);
     const unsigned grid = static_cast<unsigned>(tiles < 16384 ? (tiles > 0 ? tiles : 1) : 16384);
     wgrad_reduce_many_kernel<8><<<grid, 256, 0, s>>>(ws, splits, split_stride, ws_ld, rows, cols,
                                                      swapped, K, RS, C, cpad, dW, dw_dtype, cin,
-                                                     alpha, beta);
+                                                     alpha, beta, remap);
     return cudaGetLastError();
   }
   // every split group gets at least two splits, so two loads per row are in flight
@@ -498,11 +529,11 @@ cudaError_t launch_wgrad_reduce(const float* ws, int splits, long long split_str
     if (swapped)                                                                                \
       wgrad_reduce_kernel<GG, true><<<grid, 256, 0, s>>>(ws, splits, split_stride, ws_ld, rows, \
                                                          cols, K, RS, C, cpad, dW, dw_dtype,    \
-                                                         cin, alpha, beta);                     \
+                                                         cin, alpha, beta, remap);              \
     else                                                                                        \
       wgrad_reduce_kernel<GG, false><<<grid, 256, 0, s>>>(ws, splits, split_stride, ws_ld,      \
                                                           rows, cols, K, RS, C, cpad, dW,       \
-                                                          dw_dtype, cin, alpha, beta);          \
+                                                          dw_dtype, cin, alpha, beta, remap);   \
   } while (0)
   switch (G) {
     case 4: IGC_REDUCE(4); break;
@@ -823,6 +854,100 @@ cudaError_t launch_filter_taps8(const void* w, void* dst, int K, int RS, int C, 
   if (blocks > 16384) blocks = 16384;
   filter_taps8_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
       static_cast<const uint16_t*>(w), static_cast<uint4*>(dst), K, RS, C, bn, tiles_n, total);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Few-channel packing (FewPack in igconv_internal.h), 16-bit element copies,
+// one 8-element (16-byte) output vector per thread:
+//   few_pack_x:      X[N][H][W][C] -> Zp[N][Hz][Wz][cz] (space-to-depth by the
+//                    strides, zero padding stored)
+//   few_pack_filter: W[K][R][S][C] -> Wpk[K][R2 * Sv][64], each virtual
+//                    channel the filter entry few_pack_decode names, or zero
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint4 pack8_u16(const uint16_t v[8]) {
+  return make_uint4(v[0] | (static_cast<uint32_t>(v[1]) << 16),
+                    v[2] | (static_cast<uint32_t>(v[3]) << 16),
+                    v[4] | (static_cast<uint32_t>(v[5]) << 16),
+                    v[6] | (static_cast<uint32_t>(v[7]) << 16));
+}
+
+__global__ void __launch_bounds__(256) few_pack_x_kernel(const uint16_t* __restrict__ X,
+                                                         uint4* __restrict__ Zp, FewPack f, int H,
+                                                         int W, long long total) {
+  const int vpp = f.cz / 8;  // output vectors per packed pixel
+  const int fwc = f.fw * f.C;
+  const int used = f.fh * fwc;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    // i = ((n * Hz + zi) * Wz + zj) * vpp + v
+    const int v = static_cast<int>(i % vpp);
+    long long rest = i / vpp;
+    const int zj = static_cast<int>(rest % f.Wz);
+    rest /= f.Wz;
+    const int zi = static_cast<int>(rest % f.Hz);
+    const long long n = rest / f.Hz;
+    uint16_t o[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      const int e = v * 8 + t;
+      if (e >= used) break;
+      const int dy = e / fwc;
+      const int rem = e - dy * fwc;
+      const int dx = rem / f.C;
+      const int c = rem - dx * f.C;
+      const int h = f.fh * (zi + f.A0) + dy;
+      const int w = f.fw * (zj + f.B0) + dx;
+      if (h >= 0 && h < H && w >= 0 && w < W)
+        o[t] = X[((n * H + h) * W + w) * f.C + c];
+    }
+    Zp[i] = pack8_u16(o);
+  }
+}
+
+__global__ void __launch_bounds__(256) few_pack_filter_kernel(const uint16_t* __restrict__ Wt,
+                                                              uint4* __restrict__ Wpk, FewPack f,
+                                                              long long total) {
+  const int vts = f.R2 * f.Sv;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    // i = (k * vts + vt) * 8 + v
+    const int v = static_cast<int>(i & 7);
+    const long long rest = i >> 3;
+    const int vt = static_cast<int>(rest % vts);
+    const long long k = rest / vts;
+    uint16_t o[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      int tap, c;
+      if (few_pack_decode(f, vt, v * 8 + t, &tap, &c))
+        o[t] = Wt[(k * f.R * f.S + tap) * f.C + c];
+    }
+    Wpk[i] = pack8_u16(o);
+  }
+}
+
+cudaError_t launch_few_pack_x(const void* X, void* Zp, const FewPack& f, int N, int H, int W,
+                              cudaStream_t s) {
+  if (f.cz < 8 || f.cz > 64 || f.C < 1 || f.C > 8) return cudaErrorInvalidValue;
+  const long long total = static_cast<long long>(N) * f.Hz * f.Wz * (f.cz / 8);
+  long long blocks = (total + 255) / 256;
+  if (blocks < 1) blocks = 1;
+  if (blocks > 65536) blocks = 65536;
+  few_pack_x_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+      static_cast<const uint16_t*>(X), static_cast<uint4*>(Zp), f, H, W, total);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_few_pack_filter(const void* Wt, void* Wpk, const FewPack& f, int K,
+                                   cudaStream_t s) {
+  if (f.cz < 8 || f.cz > 64 || f.C < 1 || f.C > 8) return cudaErrorInvalidValue;
+  const long long total = static_cast<long long>(K) * f.R2 * f.Sv * 8;
+  long long blocks = (total + 255) / 256;
+  if (blocks < 1) blocks = 1;
+  if (blocks > 16384) blocks = 16384;
+  few_pack_filter_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+      static_cast<const uint16_t*>(Wt), static_cast<uint4*>(Wpk), f, total);
   return cudaGetLastError();
 }
 

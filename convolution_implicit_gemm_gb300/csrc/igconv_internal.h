@@ -147,13 +147,57 @@ cudaError_t launch_conv_gemm(const ConvGemmParams& p, int block_n, int grid, cud
 int conv_gemm_pair_capacity(int block_n);
 size_t conv_gemm_smem_bytes(int block_n);
 
+// Few-channel packing (C <= 8, dilation 1).  X is copied once to a padded
+// space-to-depth image Zp[N][Hz][Wz][cz]: packed pixel (i, j) holds the
+// fh x fw input pixels (fh*(i + A0) + dy, fw*(j + B0) + dx), channel
+// e = (dy * fw + dx) * C + c, zero past fh*fw*C channels and outside the
+// input (fh, fw = the strides; cz = 8, 16, 32 or 64).  An im2col map whose
+// pixel stride is one packed pixel (cz * 2 bytes) but whose channel box is
+// 64 elements then reads ppr = 64 / cz consecutive packed pixels as one
+// 128-byte row, so the convolution is a stride-1 one over 64 "channels"
+// with R2 x Sv taps, the Sv taps along w ppr packed pixels apart.  Virtual
+// channel ev of virtual tap vt = r2 * Sv + sv is packed pixel jp = ev / cz of
+// the window, channel ev % cz; few_pack_decode maps it back to the filter
+// tap (r * S + s) and channel it multiplies, or reports a zero slot.
+struct FewPack {
+  int fh, fw;      // space-to-depth factors (the strides)
+  int C, R, S;     // the real problem's channels and filter
+  int ph, pw;      // its padding
+  int cz, ppr;     // channels per packed pixel; packed pixels per 128-byte row
+  int A0, B0;      // packed-row / -column offset of virtual tap 0: floor(-pad / f)
+  int R2, Sv;      // virtual taps along h and along w
+  int Hz, Wz, Wv;  // packed rows, packed columns, window starts along w
+};
+
+__host__ __device__ inline bool few_pack_decode(const FewPack& f, int vt, int ev, int* tap,
+                                                int* c) {
+  const int r2 = vt / f.Sv;
+  const int sv = vt - r2 * f.Sv;
+  const int jp = ev / f.cz;
+  const int e = ev - jp * f.cz;
+  const int fwc = f.fw * f.C;
+  if (e >= f.fh * fwc) return false;
+  const int dy = e / fwc;
+  const int rem = e - dy * fwc;
+  const int dx = rem / f.C;
+  const int r = f.fh * (r2 + f.A0) + dy + f.ph;
+  const int s = f.fw * (sv * f.ppr + jp + f.B0) + dx + f.pw;
+  if (r < 0 || r >= f.R || s < 0 || s >= f.S) return false;
+  *tap = r * f.S + s;
+  *c = rem - dx * f.C;
+  return true;
+}
+
 // Auxiliary kernels (aux_kernels.cu).
 cudaError_t launch_batched_transpose(const void* src, void* dst, long long batch, long long rows,
                                      long long cols, int elem_bytes, cudaStream_t s);
+// rows / columns of the partials are (tap, c) with c < cpad, or, when
+// remap is given, few-channel virtual rows (vt * 64 + ev) decoded by
+// few_pack_decode
 cudaError_t launch_wgrad_reduce(const float* ws, int splits, long long split_stride, int ws_ld,
                                 int rows, int cols, int swapped, int K, int RS, int C, int cpad,
                                 void* dW, int dw_dtype, const void* cin, float alpha, float beta,
-                                cudaStream_t s);
+                                cudaStream_t s, const FewPack* remap = nullptr);
 cudaError_t launch_conv_splitk_reduce(const float* ws, int splits, long long split_stride,
                                       int ws_ld, long long rows, int cols, void* out,
                                       int out_bf16, const void* cin, const void* bias,
@@ -168,6 +212,10 @@ cudaError_t launch_pad_pixels8(const void* src, void* dst, long long pixels, int
                                cudaStream_t s);
 cudaError_t launch_filter_taps8(const void* w, void* dst, int K, int RS, int C, int bn,
                                 cudaStream_t s);
+cudaError_t launch_few_pack_x(const void* X, void* Zp, const FewPack& f, int N, int H, int W,
+                              cudaStream_t s);
+cudaError_t launch_few_pack_filter(const void* Wt, void* Wpk, const FewPack& f, int K,
+                                   cudaStream_t s);
 cudaError_t launch_group_filter64(const void* w, void* dst, int K, int RS, int cg,
                                   cudaStream_t s);
 cudaError_t launch_group_extract64(const float* src, void* dW, int dw_dtype, const void* cin,

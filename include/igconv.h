@@ -562,6 +562,12 @@ IGCONV_API const char *igconv_status_string(igconv_status_t status);
  *                             built-in choice), n >= 2 always n (at most 16,
  *                             clamped to the reduction blocks; CTA pairs
  *                             are then not used).
+ *   IGCONV_TUNE_FEW_CHANNELS  few-channel fprop and wgrad (C <= 8): 0 the
+ *                             built-in choice (the space-to-depth packed
+ *                             path at dilation 1 when stride_h * stride_w
+ *                             * C <= 64, else the tap-packed one); 1 always
+ *                             the tap-packed path.  Query workspace sizes
+ *                             after setting it.
  * Returns INVALID_ARG for an unknown key or value. */
 typedef enum {
     IGCONV_TUNE_WGRAD_SPLITS = 1,
@@ -569,7 +575,8 @@ typedef enum {
     IGCONV_TUNE_MAX_CTAS = 3,
     IGCONV_TUNE_CTA_PAIRS = 4,
     IGCONV_TUNE_EPI_GROUPS = 5,
-    IGCONV_TUNE_CONV_SPLITS = 6
+    IGCONV_TUNE_CONV_SPLITS = 6,
+    IGCONV_TUNE_FEW_CHANNELS = 7
 } igconv_tune_key_t;
 IGCONV_API igconv_status_t igconv_set_tuning(igconv_tune_key_t key, int value);
 

@@ -163,6 +163,9 @@ def test_tuning_keys(igc):
     assert lib.igconv_set_tuning(igc.TUNE_CTA_PAIRS, 2) == 0
     assert lib.igconv_set_tuning(igc.TUNE_CTA_PAIRS, 1) == 0
     assert lib.igconv_set_tuning(igc.TUNE_CTA_PAIRS, 0) == 0
+    assert lib.igconv_set_tuning(igc.TUNE_FEW_CHANNELS, 2) == 1
+    assert lib.igconv_set_tuning(igc.TUNE_FEW_CHANNELS, 1) == 0
+    assert lib.igconv_set_tuning(igc.TUNE_FEW_CHANNELS, 0) == 0
 
 
 def test_grouped_reject_invalid(igc):

@@ -4,10 +4,14 @@ TMA row.
 
 dgrad runs the dense data gradient over the filter padded to 8 channels,
 writes alpha * acc as fp32 rows of 8 channels in the workspace, and a second
-kernel finishes the C real channels (beta * Cin, the cast).  wgrad copies the
-pixels to 8-channel rows in the workspace and packs 8 filter taps x 8
-channels into each 64-row reduction operand, so a 7x7 filter takes 7 chunks
-instead of 49; the ordered split reduction writes the C real channels.
+kernel finishes the C real channels (beta * Cin, the cast).  wgrad has two
+paths.  At dilation 1 (stride_h * stride_w * C <= 64) the pixels are packed
+by space-to-depth into a padded image whose 128-byte windows of consecutive
+packed pixels form the reduction operand's rows.  Otherwise (or with
+IGCONV_TUNE_FEW_CHANNELS = 1) the pixels are copied to 8-channel rows and
+each 64-row operand block packs 8 filter taps x 8 channels.  Either way the
+ordered split reduction maps the rows back to (tap, channel) and writes the
+C real channels.
 """
 import numpy as np
 import pytest
@@ -34,7 +38,20 @@ SHAPES = [
     problem(2, 10, 10, 6, 256, 2, 2, (1, 1)),                      # 4 taps, wide K
     problem(1, 12, 14, 3, 384, 3, 3, (1, 1)),                      # 9 taps, wide K
     problem(2, 11, 10, 7, 24, 3, 5, (1, 2), (2, 3), (2, 1)),       # stride + dilation mix
+    problem(2, 40, 44, 3, 64, 11, 11, (2, 2), (4, 4)),             # 11x11 stride 4
+    problem(2, 32, 32, 3, 96, 4, 4, (0, 0), (4, 4)),               # 4x4 patches, stride 4
+    problem(1, 19, 23, 4, 32, 9, 9, (4, 4)),                       # 9 taps along w
+    problem(2, 21, 20, 7, 24, 3, 5, (1, 2), (2, 3)),               # strides 2 x 3
+    problem(2, 13, 12, 5, 16, 3, 3, (3, 0), (1, 2)),               # pad 3 > R - 1
 ]
+FEW_PATHS = {0: "packed", 1: "taps"}
+
+
+@pytest.fixture(params=list(FEW_PATHS), ids=FEW_PATHS.get)
+def few_mode(request):
+    igc.igconv_set_tuning(igc.TUNE_FEW_CHANNELS, request.param)
+    yield request.param
+    igc.igconv_set_tuning(igc.TUNE_FEW_CHANNELS, 0)
 
 
 def _id(p):
@@ -83,7 +100,7 @@ def test_dgrad_integer_exact(pb):
 
 @pytest.mark.parametrize("pb", SHAPES, ids=_id)
 @pytest.mark.parametrize("dw_dtype", ["f32", "f16"])
-def test_wgrad_integer_exact(pb, dw_dtype):
+def test_wgrad_integer_exact(pb, dw_dtype, few_mode):
     inp, P, Q = inputs(pb, "f16", "int_uniform", 137, cin=True, dw_dtype=dw_dtype)
     for alpha, beta in [(1.0, 0.0), (0.5, 1.0)]:
         got = run_wgrad(pb, inp, "f16", dw_dtype, alpha, beta)
@@ -93,8 +110,8 @@ def test_wgrad_integer_exact(pb, dw_dtype):
         assert_exact(got, ref, dw_dtype, f"few-channel wgrad {dw_dtype} beta={beta}")
 
 
-@pytest.mark.parametrize("pb", [SHAPES[0], SHAPES[2], SHAPES[7], SHAPES[9]], ids=_id)
-def test_random_normal_bf16(pb):
+@pytest.mark.parametrize("pb", [SHAPES[0], SHAPES[2], SHAPES[7], SHAPES[9], SHAPES[10]], ids=_id)
+def test_random_normal_bf16(pb, few_mode):
     inp, P, Q = inputs(pb, "bf16", "normal_he", 139, dw_dtype="f32")
     got = run_dgrad(pb, inp, "bf16")
     ref, A = oracle.dgrad(pb, f64(inp["dY"]), f64(inp["W"]), want_abs=True)
@@ -104,7 +121,7 @@ def test_random_normal_bf16(pb):
     assert_close(got, ref, A, "f32", "normal few-channel wgrad")
 
 
-def test_tile_width_and_split_knobs_agree():
+def test_tile_width_and_split_knobs_agree(few_mode):
     """Every forced tile width and split count gives the same integer dW."""
     pb = SHAPES[0]
     inp, P, Q = inputs(pb, "f16", "int_uniform", 149)
@@ -121,7 +138,7 @@ def test_tile_width_and_split_knobs_agree():
         igc.igconv_set_tuning(igc.TUNE_WGRAD_SPLITS, 0)
 
 
-def test_unaligned_rows_accepted():
+def test_unaligned_rows_accepted(few_mode):
     """Rows of C < 8 channels are never 16-byte aligned in general: X, W, dX
     and dW one element past a 16-byte boundary are accepted."""
     pb = SHAPES[0]

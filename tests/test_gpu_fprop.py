@@ -194,21 +194,39 @@ def test_cta_pairs_256_bit_identical(pb):
     np.testing.assert_array_equal(out[2], out[1])
 
 
-# Few input channels (C <= 8): the first layer of a CNN.  Pixels are copied
-# to 8-channel rows and the filter to [tap][k][8] in the workspace, and a
-# reduction block packs 8 taps x 8 channels.
+# Few input channels (C <= 8): the first layer of a CNN.  Two paths: at
+# dilation 1 (and stride_h * stride_w * C <= 64) the pixels are packed by
+# space-to-depth into a padded image read as 128-byte windows of consecutive
+# packed pixels; otherwise (or with IGCONV_TUNE_FEW_CHANNELS = 1) pixels are
+# copied to 8-channel rows and a reduction block packs 8 taps x 8 channels.
 FEW_SHAPES = [
     problem(2, 32, 32, 3, 64, 7, 7, (3, 3), (2, 2)),             # stem: 7x7 stride 2
     problem(1, 17, 13, 1, 16, 3, 3, (1, 1)),                      # one channel, ragged M
     problem(3, 15, 15, 4, 40, 5, 5, (4, 4), (1, 1), (2, 2)),      # dilation 2, 25 taps
     problem(2, 9, 11, 8, 136, 3, 3, (1, 1), (2, 1)),              # C = 8, K past one tile
     problem(1, 6, 6, 3, 8, 1, 1),                                 # 1x1, one padded block
+    problem(2, 40, 44, 3, 64, 11, 11, (2, 2), (4, 4)),            # 11x11 stride 4: 64-ch pixels
+    problem(2, 32, 32, 3, 96, 4, 4, (0, 0), (4, 4)),              # 4x4 patches, stride 4
+    problem(1, 19, 23, 4, 32, 9, 9, (4, 4)),                      # 9 taps along w: 2 windows
+    problem(2, 21, 20, 7, 24, 3, 5, (1, 2), (2, 3)),              # strides 2 x 3, 7 channels
+    problem(1, 17, 16, 2, 8, 2, 2, (0, 0), (3, 3)),               # stride 3 > R
+    problem(2, 13, 12, 5, 16, 3, 3, (3, 0), (1, 2)),              # pad 3 > R - 1
 ]
+FEW_PATHS = {0: "packed", 1: "taps"}
 
 
+@pytest.mark.parametrize("mode", FEW_PATHS, ids=FEW_PATHS.get)
 @pytest.mark.parametrize("pb", FEW_SHAPES, ids=lambda p: "x".join(str(p[k]) for k in "NHWCKRS") +
                          f"_s{p['stride_h']}{p['stride_w']}_d{p['dil_h']}{p['dil_w']}")
-def test_few_channels(pb):
+def test_few_channels(pb, mode):
+    try:
+        igc.igconv_set_tuning(igc.TUNE_FEW_CHANNELS, mode)
+        _few_channels_case(pb)
+    finally:
+        igc.igconv_set_tuning(igc.TUNE_FEW_CHANNELS, 0)
+
+
+def _few_channels_case(pb):
     P, Q = igc.conv2d_output_size(pb)
     assert igc.conv2d_fprop_workspace_size(pb, torch.float16) > 0
     iinp, _, _ = inputs(pb, "f16", "int_uniform", 41, bias=True)
