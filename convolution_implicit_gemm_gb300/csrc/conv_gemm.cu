@@ -14,10 +14,11 @@
 //          spread over several TMEM accumulators so that every fp32 partial
 //          sum stays an exactly representable integer
 //
-// Roles inside one CTA (448 threads, one CTA per SM):
+// Roles inside one CTA (512 threads = four warpgroups, one CTA per SM):
 //   warps 0-3, lane 0  TMA producers (3 or 4 of them): fill a ring of
 //                      shared-memory stages, each issuing every NP-th stage
-//   warps 12-13, lane 0 MMA issuers (warp 12 also allocates TMEM).  One
+//   warps 12-13, lane 0 MMA issuers (warp 12 also allocates TMEM; warps 14-15
+//                      only take part in the register split).  One
 //                      thread can issue a tcgen05.mma only every ~70 cycles,
 //                      while an M=128, N=128, K=16 MMA executes in 64, so
 //                      tiles narrower than 256 use two issuers that take
@@ -27,6 +28,11 @@
 //                      one half of the tile's columns, applies the fused
 //                      math, stages rows in shared memory and writes them
 //                      back with coalesced 16-byte stores
+// Registers: the CTA launches at 128 per thread (the most 512 threads may
+// have), then the producer and MMA warpgroups give back 40 each and the two
+// epilogue warpgroups take 168, the count their unrolled TMEM-to-global
+// paths need without spilling (at 128, as with 448 threads where some SMSPs
+// hold four warps, they spilled ~100 bytes per thread to local memory).
 // TMEM holds two accumulator buffers so the epilogue of one tile overlaps
 // the main loop of the next.  Every mbarrier wait is bounded; on a timeout
 // the CTA records an error code, stops issuing work, waits for its copies
@@ -47,6 +53,12 @@ namespace igc {
 constexpr int kEpiWarps = 8;        // epilogue warps 4..11
 constexpr int kEpiWarp0 = 4;
 constexpr int kMmaWarp0 = 12;       // MMA issuer warps 12..13 (warp 12 owns TMEM)
+constexpr int kLaunchRegs = 65536 / kThreads;  // registers per thread at launch: 128
+constexpr int kRegsLow = 88;   // producer and MMA warpgroups after setmaxnreg.dec
+constexpr int kRegsEpi = 168;  // each epilogue warpgroup after setmaxnreg.inc
+// the four warpgroups' shares must add up to exactly what the CTA launched
+// with, or an inc would wait for registers that never come back
+static_assert(2 * kRegsLow + 2 * kRegsEpi == 4 * kLaunchRegs, "register split != launch pool");
 constexpr int kStagePitch = 80;     // bytes per staged row (coalesced-store path)
 constexpr int kStageBufBytes = 2048;               // one 32-row staging buffer (TMA path)
 constexpr int kStageWarpBytes = 2 * kStageBufBytes; // double-buffered per epilogue warp
@@ -1471,7 +1483,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp < C::NP) {
+  // Each warpgroup resizes its registers first thing in its role branch, so
+  // that all of the role's code is compiled under the new limit.
+  if (warp < 4) {
+    setmaxnreg_dec<kRegsLow>();
+    if (warp < C::NP) {
     if (warp == 0 && lane == 0) {
       for (int i = 0; i < p.nsub; ++i)
         if (p.mapA_valid & (1u << i)) tma_prefetch_map(&p.mapA[i]);
@@ -1496,11 +1512,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
     run_producer<BN, PAIR, VOL>(p, pipe, full, empty, abort_flag, warp, lane);
-  } else if (warp >= kMmaWarp0 && warp < kMmaWarp0 + C::NI) {
-    if (!PAIR || rank == 0)
+    }
+  } else if (warp >= kMmaWarp0) {
+    setmaxnreg_dec<kRegsLow>();
+    if (warp < kMmaWarp0 + C::NI && (!PAIR || rank == 0))
       run_mma<BN, PAIR>(p, pipe, full, empty, tfull, tempty, &done_bar[warp - kMmaWarp0],
                         tmem_base, abort_flag, warp - kMmaWarp0, lane);
-  } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + kEpiWarps) {
+  } else {
+    setmaxnreg_inc<kRegsEpi>();
     run_epilogue<BN, PAIR, VOL>(p, tfull, tempty, tmem_base, abort_flag, warp, stage_buf, bias_s);
   }
 
@@ -1518,6 +1537,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// The register split assumes the kernel was compiled at exactly
+// kLaunchRegs per thread (the pool the warpgroups divide); any other count
+// is refused before launch instead of risking an inc that cannot complete.
+static cudaError_t check_launch_regs(const void* kernel) {
+  cudaFuncAttributes fa;
+  const cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
+  if (e != cudaSuccess) return e;
+  return fa.numRegs == kLaunchRegs ? cudaSuccess : cudaErrorInvalidConfiguration;
+}
+
 template <int BN, bool PAIR>
 static cudaError_t launch_bn(const ConvGemmParams& p, int grid, cudaStream_t s) {
   const int smem = Cfg<BN, PAIR>::SMEM;
@@ -1525,13 +1554,17 @@ static cudaError_t launch_bn(const ConvGemmParams& p, int grid, cudaStream_t s) 
     // 3D problems take the kernel with the volume paths compiled in
     const bool vol = p.a_src == SRC_IM2COL_K3 || p.wg_Do > 0;
     auto* k = vol ? conv_gemm_kernel<BN, false, true> : conv_gemm_kernel<BN, false, false>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = check_launch_regs(reinterpret_cast<const void*>(k));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     k<<<grid, kThreads, smem, s>>>(p);
     return cudaGetLastError();
   }
-  cudaError_t e = cudaFuncSetAttribute(conv_gemm_kernel<BN, true, false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = check_launch_regs(reinterpret_cast<const void*>(conv_gemm_kernel<BN, true, false>));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(conv_gemm_kernel<BN, true, false>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   if (grid < 2 || (grid & 1)) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};

@@ -15,7 +15,7 @@ constexpr int kBlockM = 128;
 constexpr int kBlockK = 64;
 constexpr int kBiasCacheBytes = 2048;  // bias vectors up to this size are staged in shared memory
 constexpr int kMaxSub = 16;      // dgrad stride decomposition: stride_h * stride_w <= 16
-constexpr int kThreads = 448;    // warps 0-3 TMA producers, 4-11 epilogue, 12-13 MMA issuers
+constexpr int kThreads = 512;    // warps 0-3 TMA producers, 4-11 epilogue, 12-13 MMA issuers
 
 // Where an operand tile comes from, and its shared-memory major-ness.
 enum SrcKind : int {

@@ -15,6 +15,18 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 }
 
 // True in exactly one lane of a converged warp (elect.sync over all lanes).
+// Register reallocation between warpgroups (all four warps of a warpgroup
+// execute it together): dec returns registers above N to the CTA's pool,
+// inc waits until N registers per thread are available from it.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 __device__ __forceinline__ bool elect_one_sync() {
   uint32_t pred = 0;
   asm volatile(
