@@ -668,7 +668,8 @@ def fprop_int8(prob, X, Wt, bias, act_scale, w_scale, out_scale, relu=True, out=
 def grouped_fprop(prob, groups, X, Wt, bias=None, Cin=None, alpha=1.0, beta=0.0, relu=False,
                   out=None, stream=None):
     """Grouped fprop; allocates the workspace that opens the tensor-core path
-    (group widths 4..64) or the few-channel path (groups = 1, C <= 8)."""
+    (C == K with group widths from 4, C != K with whole groups per 64-wide
+    tile) or the few-channel path (groups = 1, C <= 8)."""
     pb = Problem.make(prob)
     P, Q = conv2d_output_size(pb)
     Y = out if out is not None else torch.empty((pb.N, P, Q, pb.K), dtype=X.dtype, device=X.device)
@@ -684,7 +685,8 @@ def grouped_fprop(prob, groups, X, Wt, bias=None, Cin=None, alpha=1.0, beta=0.0,
 
 def grouped_dgrad(prob, groups, dY, Wt, Cin=None, alpha=1.0, beta=0.0, out=None, stream=None):
     """Grouped dgrad; allocates the workspace that opens the tensor-core path
-    (group widths 4..64)."""
+    (C == K with group widths from 4, C != K with whole groups per 64-wide
+    tile)."""
     pb = Problem.make(prob)
     dX = out if out is not None else torch.empty((pb.N, pb.H, pb.W, pb.C), dtype=dY.dtype,
                                                  device=dY.device)

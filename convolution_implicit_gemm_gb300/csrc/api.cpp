@@ -690,14 +690,42 @@ void plan_wgrad_taps(const igconv_problem_t* pb, int P, int Q, int sm_count, Wgr
   choose_wgrad_shape(pb->K, static_cast<long long>(ceil_div(w->rs, 8)) * kBlockK, sm_count, w, 256);
 }
 
-// Grouped wgrad as a block-diagonal GEMM (C == K, group width 4..64): rows
-// (tap, c') with c' < 64 inside the output tile's channel block, one 64-wide
-// column tile per channel block; the split rule of plan_wgrad_shape.
-void plan_wgrad_grouped(const igconv_problem_t* pb, int P, int Q, int sm_count, WgradPlan* w) {
+// Channel window of a grouped block-diagonal GEMM whose 64-wide tiles run
+// over groups of tile_g channels (K / groups for fprop and wgrad, C / groups
+// for dgrad) and reduce over red_g channels per group on the other side:
+// every tile holds whole groups, so tile n reduces over the `width` channels
+// starting at (n / div) * mul.  False when a tile would split a group or a
+// window start is not a multiple of 8 channels (a TMA copy's channel
+// coordinate must be 16-byte aligned).
+struct GroupWin {
+  int mul, div, width, blocks;
+};
+bool plan_group_window(int tile_g, int red_g, GroupWin* g) {
+  if (tile_g < 1 || red_g < 1) return false;
+  if (64 % tile_g == 0) {  // 64 / tile_g groups per tile
+    g->div = 1;
+    g->mul = 64 / tile_g * red_g;
+  } else if (tile_g % 64 == 0) {  // tile_g / 64 tiles per group
+    g->div = tile_g / 64;
+    g->mul = red_g;
+  } else {
+    return false;
+  }
+  if (g->mul % 8 != 0) return false;
+  g->width = g->mul;
+  g->blocks = ceil_div(g->width, kBlockK);
+  return true;
+}
+
+// Grouped wgrad as a block-diagonal GEMM: rows (tap, c') with c' inside the
+// output tile's channel window (win.blocks 64-channel blocks), one 64-wide
+// column tile per 64 output channels; the split rule of plan_wgrad_shape.
+void plan_wgrad_grouped(const igconv_problem_t* pb, int P, int Q, int sm_count,
+                        const GroupWin& win, WgradPlan* w) {
   const int sms = sm_count > 0 ? sm_count : 148;
   w->rs = pb->R * pb->S;
-  w->cblocks = 1;
-  w->cpad = kBlockK;
+  w->cblocks = win.blocks;
+  w->cpad = win.blocks * kBlockK;
   const long long xext = static_cast<long long>(w->rs) * w->cpad;
   const long long npq = static_cast<long long>(pb->N) * P * Q;
   w->kblocks = ceil_div(npq, kBlockK);
@@ -721,9 +749,10 @@ void plan_wgrad_grouped(const igconv_problem_t* pb, int P, int Q, int sm_count, 
 }
 
 // Workspace of the grouped wgrad GEMM: the split partials, then the fp32
-// gradient of the block-local filter [K][R][S][64].
+// gradient of the windowed filter [K][R][S][cpad].
 size_t grouped_wgrad_gemm_bytes(const WgradPlan& w, const igconv_problem_t* pb) {
-  return round256(w.ws_bytes) + round256(static_cast<size_t>(pb->K) * w.rs * 64 * sizeof(float));
+  return round256(w.ws_bytes) +
+         round256(static_cast<size_t>(pb->K) * w.rs * w.cpad * sizeof(float));
 }
 
 // ---------------------------------------------------------------------------
@@ -756,7 +785,8 @@ bool encode_nhwc_window(CUtensorMap* map, const void* base, int bf16, int n, int
 // Common checks of the grouped entry points.  groups == 1 is the dense path
 // (*direct = false).  Otherwise the direct kernels cover C == K with a group
 // width C/groups of 1 (depthwise), 2, 4, 8, 16 or 32 (*direct = true,
-// *cg = C/groups); other group counts are UNSUPPORTED.
+// *cg = C/groups); other group counts (C != K among them) are UNSUPPORTED
+// here and run only on the tensor-core path (grouped_gemm_ok).
 igconv_status_t check_groups(const igconv_problem_t* prob, int groups, bool* direct, int* cg) {
   if (!prob || groups < 1) return IGCONV_ERR_INVALID_ARG;
   if (prob->C < 1 || prob->K < 1 || prob->C % groups != 0 || prob->K % groups != 0)
@@ -1700,14 +1730,28 @@ igconv_status_t conv2d_grouped_fprop(const igconv_problem_t* prob, int groups,
   return from_cuda(launch_depthwise(p, grid, static_cast<cudaStream_t>(stream)));
 }
 
-// Grouped fprop on the tensor cores (C == K, group width 4..64 dividing
-// 64): an implicit GEMM over 64-channel blocks in which output tile n (64
-// channels, BN = 64) reduces over the filter taps of input block n only,
-// against a block-diagonal filter image built in the workspace.
-static bool grouped_gemm_width(const igconv_problem_t* prob, int groups) {
-  if (!prob || groups < 2 || prob->C != prob->K || prob->C % groups != 0) return false;
-  const int cg = prob->C / groups;
-  return cg == 4 || cg == 8 || cg == 16 || cg == 32 || cg == 64;
+// Grouped convolution on the tensor cores: an implicit GEMM with 64-wide
+// tiles of whole groups, tile n reducing over its group window of the
+// other side's channels (plan_group_window) against a dense block-diagonal
+// filter image [K][R][S][C] in the workspace.  Any C / K ratio whose windows
+// plan_group_window accepts (multiples of 8 channels); for C == K the
+// widths 1 and 2 stay with the direct kernels.  dgrad's tiles run over C,
+// fprop's and wgrad's over K.
+static bool grouped_gemm_ok(const igconv_problem_t* prob, int groups, bool dgrad,
+                            GroupWin* win = nullptr) {
+  if (!prob || groups < 2 || prob->C < 1 || prob->K < 1) return false;
+  if (prob->C % groups != 0 || prob->K % groups != 0) return false;
+  if (prob->C % 8 != 0 || prob->K % 8 != 0) return false;
+  const int cg = prob->C / groups, kg = prob->K / groups;
+  if (prob->C == prob->K && cg < 4) return false;
+  GroupWin w;
+  if (!plan_group_window(dgrad ? cg : kg, dgrad ? kg : cg, &w)) return false;
+  if (win) *win = w;
+  return true;
+}
+
+static size_t grouped_filter_bytes(const igconv_problem_t* prob) {
+  return round256(static_cast<size_t>(prob->K) * prob->R * prob->S * prob->C * 2);
 }
 
 size_t conv2d_grouped_fprop_workspace_size(const igconv_problem_t* prob, int groups,
@@ -1715,8 +1759,8 @@ size_t conv2d_grouped_fprop_workspace_size(const igconv_problem_t* prob, int gro
   if (dtype != IGCONV_F16 && dtype != IGCONV_BF16) return 0;
   if (!prob || groups < 1 || prob->C < 1 || prob->K < 1 || prob->R < 1 || prob->S < 1) return 0;
   if (groups == 1) return conv2d_fprop_workspace_size(prob, dtype);
-  if (!grouped_gemm_width(prob, groups)) return 0;
-  return round256(static_cast<size_t>(prob->K) * prob->R * prob->S * 64 * 2);
+  if (!grouped_gemm_ok(prob, groups, false)) return 0;
+  return grouped_filter_bytes(prob);
 }
 
 igconv_status_t conv2d_grouped_fprop_ws(const igconv_problem_t* prob, int groups,
@@ -1730,7 +1774,8 @@ igconv_status_t conv2d_grouped_fprop_ws(const igconv_problem_t* prob, int groups
                            workspace_bytes, stream);
   if (prob->C < 1 || prob->K < 1 || prob->C % groups != 0 || prob->K % groups != 0)
     return IGCONV_ERR_INVALID_ARG;
-  if (!grouped_gemm_width(prob, groups))  // depthwise, width 2, or uncovered
+  GroupWin win;
+  if (!grouped_gemm_ok(prob, groups, false, &win))  // depthwise, width 2, or uncovered
     return conv2d_grouped_fprop(prob, groups, dtype, X, Wt, bias, Cin, Y, alpha, beta, relu,
                                 stream);
   int P = 0, Q = 0;
@@ -1748,19 +1793,19 @@ igconv_status_t conv2d_grouped_fprop_ws(const igconv_problem_t* prob, int groups
   DeviceState* dev = nullptr;
   if ((st = device_state(&dev)) != IGCONV_OK) return st;
   const int bf16 = dtype == IGCONV_BF16 ? 1 : 0;
-  const int cg = prob->C / groups;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  if (launch_group_filter64(Wt, workspace, prob->K, prob->R * prob->S, cg, cs) != cudaSuccess)
+  if (launch_group_filter_dense(Wt, workspace, prob->K, prob->R * prob->S, prob->C,
+                                prob->C / groups, prob->K / groups, cs) != cudaSuccess)
     return IGCONV_ERR_CUDA;
   constexpr int bn = 64;
   ConvGemmParams p;
   init_common(p, dev);
+  // the dense plan over the block-diagonal filter, with each tile's
+  // reduction cut down to its group window
   if ((st = plan_fprop(p, bn, prob, P, Q, bf16, X, workspace)) != IGCONV_OK) return st;
-  // one 64-channel block per tap: input block n for output tile n
-  p.cblocks = 1;
-  p.a_cb_per_tn = 1;
-  if (!encode_filter(&p.mapB, workspace, bf16, prob->K, prob->R, prob->S, 64, bn))
-    return IGCONV_ERR_UNSUPPORTED;
+  p.cblocks = win.blocks;
+  p.grp_mul = win.mul;
+  p.grp_div = win.div;
   p.epi = EPI_STORE;
   p.out = Y;
   set_out_map_16(p, Y, static_cast<long long>(prob->N) * P * Q, prob->K, bf16, bn,
@@ -1829,8 +1874,8 @@ size_t conv2d_grouped_dgrad_workspace_size(const igconv_problem_t* prob, int gro
                                            igconv_dtype_t dtype) {
   if (dtype != IGCONV_F16 && dtype != IGCONV_BF16) return 0;
   if (!prob || groups < 2 || prob->R < 1 || prob->S < 1) return 0;
-  if (!grouped_gemm_width(prob, groups)) return 0;
-  return round256(static_cast<size_t>(prob->K) * prob->R * prob->S * 64 * 2);
+  if (!grouped_gemm_ok(prob, groups, true)) return 0;
+  return grouped_filter_bytes(prob);
 }
 
 // Grouped dgrad on the tensor cores: the dgrad implicit GEMM (residue-class
@@ -1844,7 +1889,8 @@ igconv_status_t conv2d_grouped_dgrad_ws(const igconv_problem_t* prob, int groups
   if (!prob || groups < 1) return IGCONV_ERR_INVALID_ARG;
   if (prob->C < 1 || prob->K < 1 || prob->C % groups != 0 || prob->K % groups != 0)
     return IGCONV_ERR_INVALID_ARG;
-  if (!grouped_gemm_width(prob, groups))  // dense, depthwise, width 2, or uncovered
+  GroupWin win;
+  if (!grouped_gemm_ok(prob, groups, true, &win))  // dense, depthwise, width 2, or uncovered
     return conv2d_grouped_dgrad(prob, groups, dtype, dY, Wt, Cin, dX, alpha, beta, stream);
   int P = 0, Q = 0;
   igconv_status_t st = check_shape(prob, &P, &Q);
@@ -1862,35 +1908,39 @@ igconv_status_t conv2d_grouped_dgrad_ws(const igconv_problem_t* prob, int groups
   DeviceState* dev = nullptr;
   if ((st = device_state(&dev)) != IGCONV_OK) return st;
   const int bf16 = dtype == IGCONV_BF16 ? 1 : 0;
-  const int cg = prob->C / groups;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  if (launch_group_filter64(Wt, workspace, prob->K, prob->R * prob->S, cg, cs) != cudaSuccess)
+  if (launch_group_filter_dense(Wt, workspace, prob->K, prob->R * prob->S, prob->C,
+                                prob->C / groups, prob->K / groups, cs) != cudaSuccess)
     return IGCONV_ERR_CUDA;
   ConvGemmParams p;
   init_common(p, dev);
   int bn = 64;
+  // the dense dgrad plan over the block-diagonal filter (read MN-major),
+  // each dX channel tile reducing over its window of dY channels
   if ((st = plan_dgrad(p, &bn, prob, P, Q, bf16, dY, workspace, dev->sm_count, 64)) != IGCONV_OK)
     return st;
-  p.cblocks = 1;
-  p.a_cb_per_tn = 1;
-  if (!encode_filter(&p.mapB, workspace, bf16, prob->K, prob->R, prob->S, 64, 64))
-    return IGCONV_ERR_UNSUPPORTED;
+  p.cblocks = win.blocks;
+  p.grp_mul = win.mul;
+  p.grp_div = win.div;
   p.pf_base = workspace;
-  p.pf_bytes = static_cast<long long>(prob->K) * prob->R * prob->S * 64 * 2;
+  p.pf_bytes = static_cast<long long>(prob->K) * prob->R * prob->S * prob->C * 2;
   return launch_dgrad_plan(p, bn, prob, dX, Cin, alpha, beta, bf16, dev, cs);
 }
 
-// Grouped wgrad on the tensor cores (group width 4..64): the wgrad GEMM over
-// 64-channel blocks (X channel block n for output channels 64n..), split-K
-// partials reduced in order into the block-local filter gradient, whose
-// group entries are then copied out (with beta * Cin and the cast).
-static igconv_status_t grouped_wgrad_gemm(const igconv_problem_t* prob, int cg, int P, int Q,
+// Grouped wgrad on the tensor cores: the wgrad GEMM whose rows are (tap,
+// X channel of the output tile's group window) and whose 64-wide column
+// tiles are output channels, split-K partials reduced in order into the
+// gradient of the windowed filter [K][R][S][cpad], whose group entries are
+// then copied out (with beta * Cin and the cast).
+static igconv_status_t grouped_wgrad_gemm(const igconv_problem_t* prob, int groups, int P, int Q,
                                           int bf16, igconv_dtype_t dw_dtype, const void* X,
                                           const void* dY, const void* Cin, void* dW, float alpha,
                                           float beta, void* workspace, size_t workspace_bytes,
                                           const DeviceState* dev, cudaStream_t s) {
+  GroupWin win;
+  if (!grouped_gemm_ok(prob, groups, false, &win)) return IGCONV_ERR_UNSUPPORTED;
   WgradPlan w;
-  plan_wgrad_grouped(prob, P, Q, dev->sm_count, &w);
+  plan_wgrad_grouped(prob, P, Q, dev->sm_count, win, &w);
   if (!workspace || workspace_bytes < grouped_wgrad_gemm_bytes(w, prob))
     return IGCONV_ERR_WORKSPACE;
   ConvGemmParams p;
@@ -1904,8 +1954,9 @@ static igconv_status_t grouped_wgrad_gemm(const igconv_problem_t* prob, int cg, 
   p.splits = w.splits;
   p.kblocks_total = w.kblocks;
   p.units = w.tiles_m * w.tiles_n * w.splits;
-  p.cblocks = 1;
-  p.a_cb_per_tn = 1;
+  p.cblocks = w.cblocks;
+  p.grp_mul = win.mul;
+  p.grp_div = win.div;
   p.N_gemm = w.N_pad;
   p.idesc = make_idesc(kBlockM, w.bn, bf16, 1, 1);
   set_fp_accumulators(p, w.bn);
@@ -1938,20 +1989,22 @@ static igconv_status_t grouped_wgrad_gemm(const igconv_problem_t* prob, int cg, 
   if (e != cudaSuccess) return IGCONV_ERR_CUDA;
   float* dwexp = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + round256(w.ws_bytes));
   e = launch_wgrad_reduce(static_cast<const float*>(workspace), w.splits, p.ws_split_stride,
-                          w.N_pad, w.rs * w.cpad, prob->K, 0, prob->K, w.rs, kBlockK, w.cpad,
+                          w.N_pad, w.rs * w.cpad, prob->K, 0, prob->K, w.rs, w.cpad, w.cpad,
                           dwexp, 2, nullptr, alpha, 0.0f, s);
   if (e != cudaSuccess) return IGCONV_ERR_CUDA;
   const int dwt = dw_dtype == IGCONV_F32 ? 2 : (dw_dtype == IGCONV_BF16 ? 1 : 0);
-  return from_cuda(launch_group_extract64(dwexp, dW, dwt, beta != 0.0f ? Cin : nullptr, beta,
-                                          prob->K, w.rs, cg, s));
+  return from_cuda(launch_group_extract(dwexp, dW, dwt, beta != 0.0f ? Cin : nullptr, beta,
+                                        prob->K, w.rs, prob->C / groups, prob->K / groups,
+                                        w.cpad, win.mul, win.div, s));
 }
 
 size_t conv2d_grouped_wgrad_workspace_size(const igconv_problem_t* prob, int groups,
                                            igconv_dtype_t dtype, igconv_dtype_t dw_dtype) {
   bool direct = false;
   int cg = 1;
-  // width 64 has only the tensor-core path
-  if (check_groups(prob, groups, &direct, &cg) != IGCONV_OK && !grouped_gemm_width(prob, groups))
+  // widths above 32 and C != K have only the tensor-core path
+  if (check_groups(prob, groups, &direct, &cg) != IGCONV_OK &&
+      !grouped_gemm_ok(prob, groups, false))
     return 0;
   if (!direct) return conv2d_wgrad_workspace_size(prob, dtype, dw_dtype);
   int P = 0, Q = 0;
@@ -1959,9 +2012,10 @@ size_t conv2d_grouped_wgrad_workspace_size(const igconv_problem_t* prob, int gro
   if (dtype != IGCONV_F16 && dtype != IGCONV_BF16) return 0;
   DeviceState* dev = nullptr;
   if (device_state(&dev) != IGCONV_OK) return 0;
-  if (grouped_gemm_width(prob, groups)) {
+  GroupWin win;
+  if (grouped_gemm_ok(prob, groups, false, &win)) {
     WgradPlan w;
-    plan_wgrad_grouped(prob, P, Q, dev->sm_count, &w);
+    plan_wgrad_grouped(prob, P, Q, dev->sm_count, win, &w);
     return grouped_wgrad_gemm_bytes(w, prob);
   }
   DwParams p;
@@ -1977,8 +2031,8 @@ igconv_status_t conv2d_grouped_wgrad(const igconv_problem_t* prob, int groups,
   bool direct = false;
   int cg = 1;
   igconv_status_t st = check_groups(prob, groups, &direct, &cg);
-  // width 64 has only the tensor-core path
-  if (st != IGCONV_OK && !(st == IGCONV_ERR_UNSUPPORTED && grouped_gemm_width(prob, groups)))
+  // widths above 32 and C != K have only the tensor-core path
+  if (st != IGCONV_OK && !(st == IGCONV_ERR_UNSUPPORTED && grouped_gemm_ok(prob, groups, false)))
     return st;
   if (!direct)
     return conv2d_wgrad(prob, dtype, dw_dtype, X, dY, Cin, dW, alpha, beta, workspace,
@@ -1997,8 +2051,8 @@ igconv_status_t conv2d_grouped_wgrad(const igconv_problem_t* prob, int groups,
   DeviceState* dev = nullptr;
   if ((st = device_state(&dev)) != IGCONV_OK) return st;
   const int bf16 = dtype == IGCONV_BF16 ? 1 : 0;
-  if (grouped_gemm_width(prob, groups))
-    return grouped_wgrad_gemm(prob, cg, P, Q, bf16, dw_dtype, X, dY, Cin, dW, alpha, beta,
+  if (grouped_gemm_ok(prob, groups, false))
+    return grouped_wgrad_gemm(prob, groups, P, Q, bf16, dw_dtype, X, dY, Cin, dW, alpha, beta,
                               workspace, workspace_bytes, dev, static_cast<cudaStream_t>(stream));
   DwParams p;
   if ((st = plan_dw_wgrad(p, dev, prob, P, Q, bf16, cg)) != IGCONV_OK) return st;

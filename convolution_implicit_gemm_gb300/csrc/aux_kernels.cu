@@ -967,40 +967,42 @@ __global__ void selftest_wait_kernel(unsigned int* status, unsigned long long ti
   }
 }
 
-// Block-diagonal filter image of a grouped convolution (C == K, group
-// width cg dividing 64) for the implicit GEMM over 64-channel blocks:
-// dst[k][tap][j] (j < 64) = w[k][tap][j - o(k)] when j - o(k) lies in
-// [0, cg), else 0, with o(k) the offset of k's group inside its 64-channel
-// block.  Output tile n (channels 64n ..) then reads only input block n.
-__global__ void __launch_bounds__(256) group_filter64_kernel(const uint16_t* __restrict__ w,
-                                                             uint16_t* __restrict__ dst, int K,
-                                                             int RS, int cg) {
-  const long long total = static_cast<long long>(K) * RS * 64;
+// Dense block-diagonal filter of a grouped convolution (groups of cg input
+// and kg output channels), for the implicit GEMMs over group windows:
+// dst[k][tap][c] = w[k][tap][c - g * cg] when c lies in k's group
+// g = k / kg, else 0.
+__global__ void __launch_bounds__(256) group_filter_dense_kernel(const uint16_t* __restrict__ w,
+                                                                 uint16_t* __restrict__ dst,
+                                                                 int K, int RS, int C, int cg,
+                                                                 int kg) {
+  const long long total = static_cast<long long>(K) * RS * C;
   for (long long e = blockIdx.x * 256ll + threadIdx.x; e < total; e += 256ll * gridDim.x) {
-    const int j = static_cast<int>(e & 63);
-    const long long kt = e >> 6;
+    const long long kt = e / C;
+    const int c = static_cast<int>(e - kt * C);
     const int k = static_cast<int>(kt / RS);
-    const int tap = static_cast<int>(kt - static_cast<long long>(k) * RS);
-    const int o = (k - k % cg) & 63;  // group start inside the 64-channel block
-    const int jj = j - o;
-    dst[e] = (jj >= 0 && jj < cg) ? w[(static_cast<long long>(k) * RS + tap) * cg + jj] : 0;
+    const int jj = c - (k / kg) * cg;
+    dst[e] = (jj >= 0 && jj < cg) ? w[kt * cg + jj] : 0;
   }
 }
 
-// Inverse of the block-diagonal image for the weight gradient:
-// dW[k][tap][j] = cast(src[k][tap][o(k) + j] + beta * Cin[k][tap][j]), j < cg,
-// src the fp32 gradient of the block-local filter [K][RS][64] (alpha applied).
-__global__ void __launch_bounds__(256) group_extract64_kernel(const float* __restrict__ src,
-                                                              void* dW, int dw_dtype,
-                                                              const void* cin, float beta, int K,
-                                                              int RS, int cg) {
+// Weight gradient of a grouped convolution from the gradient of the windowed
+// filter: src [K][RS][cpad] (fp32, alpha applied) holds, for output channel
+// k of 64-wide tile n = k / 64, the gradient against the X channels of n's
+// window, which starts at (n / div) * mul; k's own cg channels start at
+// g * cg with g = k / kg.  dW[k][tap][j] = cast(src[k][tap][g * cg -
+// start + j] + beta * Cin[k][tap][j]), j < cg.
+__global__ void __launch_bounds__(256) group_extract_kernel(const float* __restrict__ src,
+                                                            void* dW, int dw_dtype,
+                                                            const void* cin, float beta, int K,
+                                                            int RS, int cg, int kg, int cpad,
+                                                            int mul, int div) {
   const long long total = static_cast<long long>(K) * RS * cg;
   for (long long e = blockIdx.x * 256ll + threadIdx.x; e < total; e += 256ll * gridDim.x) {
     const int j = static_cast<int>(e % cg);
     const long long kt = e / cg;
     const int k = static_cast<int>(kt / RS);
-    const int o = (k - k % cg) & 63;
-    float v = src[kt * 64 + o + j];
+    const int off = (k / kg) * cg - ((k >> 6) / div) * mul;
+    float v = src[kt * cpad + off + j];
     if (beta != 0.0f) {
       const float ci = dw_dtype == 2   ? static_cast<const float*>(cin)[e]
                        : dw_dtype == 1 ? __bfloat162float(static_cast<const __nv_bfloat16*>(cin)[e])
@@ -1016,22 +1018,26 @@ __global__ void __launch_bounds__(256) group_extract64_kernel(const float* __res
   }
 }
 
-cudaError_t launch_group_extract64(const float* src, void* dW, int dw_dtype, const void* cin,
-                                   float beta, int K, int RS, int cg, cudaStream_t s) {
+cudaError_t launch_group_extract(const float* src, void* dW, int dw_dtype, const void* cin,
+                                 float beta, int K, int RS, int cg, int kg, int cpad, int mul,
+                                 int div, cudaStream_t s) {
+  if (cg < 1 || kg < 1 || div < 1) return cudaErrorInvalidValue;
   const long long total = static_cast<long long>(K) * RS * cg;
   const long long blocks = (total + 255) / 256;
   const int grid = static_cast<int>(blocks < 8192 ? blocks : 8192);
-  group_extract64_kernel<<<grid, 256, 0, s>>>(src, dW, dw_dtype, cin, beta, K, RS, cg);
+  group_extract_kernel<<<grid, 256, 0, s>>>(src, dW, dw_dtype, cin, beta, K, RS, cg, kg, cpad,
+                                            mul, div);
   return cudaGetLastError();
 }
 
-cudaError_t launch_group_filter64(const void* w, void* dst, int K, int RS, int cg,
-                                  cudaStream_t s) {
-  const long long total = static_cast<long long>(K) * RS * 64;
+cudaError_t launch_group_filter_dense(const void* w, void* dst, int K, int RS, int C, int cg,
+                                      int kg, cudaStream_t s) {
+  if (cg < 1 || kg < 1) return cudaErrorInvalidValue;
+  const long long total = static_cast<long long>(K) * RS * C;
   const long long blocks = (total + 255) / 256;
   const int grid = static_cast<int>(blocks < 8192 ? blocks : 8192);
-  group_filter64_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(w),
-                                             static_cast<uint16_t*>(dst), K, RS, cg);
+  group_filter_dense_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(w),
+                                                 static_cast<uint16_t*>(dst), K, RS, C, cg, kg);
   return cudaGetLastError();
 }
 

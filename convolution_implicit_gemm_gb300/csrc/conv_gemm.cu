@@ -231,8 +231,14 @@ struct ProdCtx {       // producer scalars, in registers
   const CUtensorMap* mapA0;
   const CUtensorMap* mapB;
   const void* taps_filter;
-  int a_cb_tn;  // channel blocks per output tile column (grouped block-diagonal GEMM)
+  int grp_mul, grp_div;  // grouped block-diagonal GEMM: channel window of a tile (0: dense)
 };
+
+// First channel of the reduction window of 64-wide tile n in a grouped
+// block-diagonal GEMM (0 for a dense one).
+__device__ __forceinline__ int group_window(const ProdCtx& c, int tile_n) {
+  return c.grp_mul ? (tile_n / c.grp_div) * c.grp_mul : 0;
+}
 
 struct ProducerPos {
   int u;          // work unit
@@ -386,17 +392,17 @@ __device__ __forceinline__ void issue_stage_loads(const ProdCtx& c, const Produc
       }
       return;
     }
-    // grouped block-diagonal GEMM (a_cb_tn = 1, BN = 64): tile n reduces over
-    // channel block n of A and filter rows 64n.. of the block-local filter
-    const int gcb = cb + s.w.tile_n * c.a_cb_tn;
-    tma_load_im2col_4d(sA, s.mapA, bar, gcb * kBlockK, s.base_w, s.base_h, s.img, off_w, off_h);
+    // grouped block-diagonal GEMM (BN = 64): tile n reduces over its group
+    // window of the im2col operand's channels and the same channels of the
+    // dense block-diagonal filter (fprop: filter columns; dgrad: filter rows)
+    const int ch = group_window(c, s.w.tile_n) + cb * kBlockK;
+    tma_load_im2col_4d(sA, s.mapA, bar, ch, s.base_w, s.base_h, s.img, off_w, off_h);
     if (c.b_src == SRC_W_K) {
-      tma_load_4d(sB, c.mapB, bar, cb * kBlockK, sc, r, s.w.tile_n * BN);
+      tma_load_4d(sB, c.mapB, bar, ch, sc, r, s.w.tile_n * BN);
     } else {
-      const int n0 = c.a_cb_tn ? 0 : s.w.tile_n * BN;
 #pragma unroll
       for (int i = 0; i < BN / 64; ++i)
-        tma_load_4d(sB + i * 8192, c.mapB, bar, n0 + 64 * i, sc, r, gcb * kBlockK);
+        tma_load_4d(sB + i * 8192, c.mapB, bar, s.w.tile_n * BN + 64 * i, sc, r, ch);
     }
   } else {
     // wgrad: reduction block kb = 64 consecutive output positions (n, p, q)
@@ -461,9 +467,9 @@ __device__ __forceinline__ void issue_stage_loads(const ProdCtx& c, const Produc
                            static_cast<uint16_t>(jt * c.wg_dd));
         continue;
       }
-      // grouped block-diagonal wgrad (a_cb_tn = 1, one 64-wide dY tile): the
-      // X channel block of output-channel tile n is n
-      tma_load_im2col_4d(x_dst + i * 8192, c.mapA0, bar, (cb + y_tile * c.a_cb_tn) * kBlockK, bw,
+      // grouped block-diagonal wgrad (one 64-wide dY tile): the X channels of
+      // output-channel tile n are its group window
+      tma_load_im2col_4d(x_dst + i * 8192, c.mapA0, bar, group_window(c, y_tile) + cb * kBlockK, bw,
                          bh, n, static_cast<uint16_t>(sc * c.wg_dw),
                          static_cast<uint16_t>(r * c.wg_dh));
     }
@@ -504,7 +510,8 @@ __device__ __forceinline__ void run_producer(const ConvGemmParams& p, uint8_t* p
   c.mapA0 = &p.mapA[0];
   c.mapB = &p.mapB;
   c.taps_filter = p.taps_filter;
-  c.a_cb_tn = p.a_cb_per_tn;
+  c.grp_mul = p.grp_mul;
+  c.grp_div = p.grp_div > 0 ? p.grp_div : 1;
   const unsigned long long timeout = p.timeout_ns;
   ProducerPos pos;
   pos.u = unit_first(c.sc);

@@ -95,10 +95,11 @@ struct ConvGemmParams {
   int splits;                 // wgrad split-K factor (1 otherwise)
   int kblocks_total;          // wgrad: ceil(N*P*Q / 64)
   int cblocks;                // 64-channel blocks per tap (reduction channels; wgrad: X channels)
-  int a_cb_per_tn;            // channel blocks skipped per output tile column (1: grouped
-                              // block-diagonal GEMM, BN = 64: tile n reads A channel block n
-                              // and, in dgrad, filter rows 64n.. of a block-local filter; in
-                              // wgrad, X channel block n for output channels 64n..)
+  int grp_mul, grp_div;       // grouped block-diagonal GEMM (grp_mul != 0, BN = 64): 64-wide
+                              // tile n holds whole groups and reduces over the channel
+                              // window starting at (n / grp_div) * grp_mul (a multiple of 8)
+                              // of the im2col operand (X in fprop and wgrad, dY in dgrad)
+                              // and of the dense block-diagonal filter [K][R][S][C]
   int N_gemm;                 // valid GEMM columns
   uint32_t idesc;             // tcgen05 instruction descriptor
   int num_acc;                // TMEM accumulators per tile (issuers x groups)
@@ -216,10 +217,11 @@ cudaError_t launch_few_pack_x(const void* X, void* Zp, const FewPack& f, int N, 
                               cudaStream_t s);
 cudaError_t launch_few_pack_filter(const void* Wt, void* Wpk, const FewPack& f, int K,
                                    cudaStream_t s);
-cudaError_t launch_group_filter64(const void* w, void* dst, int K, int RS, int cg,
-                                  cudaStream_t s);
-cudaError_t launch_group_extract64(const float* src, void* dW, int dw_dtype, const void* cin,
-                                   float beta, int K, int RS, int cg, cudaStream_t s);
+cudaError_t launch_group_filter_dense(const void* w, void* dst, int K, int RS, int C, int cg,
+                                      int kg, cudaStream_t s);
+cudaError_t launch_group_extract(const float* src, void* dW, int dw_dtype, const void* cin,
+                                 float beta, int K, int RS, int cg, int kg, int cpad, int mul,
+                                 int div, cudaStream_t s);
 cudaError_t launch_wino_input(const void* X, void* V, int N, int H, int W, int C, int TH, int TW,
                               int ph, int pw, int bf16, cudaStream_t s);
 cudaError_t launch_wino_filter(const void* Wt, void* U, int K, int C, int bf16, cudaStream_t s);

@@ -282,10 +282,17 @@ IGCONV_API igconv_status_t conv2d_wgrad_noalloc(const igconv_problem_t *prob,
  * (same kernels, same bits, same errors).  C == K with a group width C/G of
  * 1 (depthwise, filters [C][R][S]), 2, 4, 8, 16 or 32 runs direct CUDA-core
  * kernels in conv2d_grouped_fprop / conv2d_grouped_dgrad: such a layer does
- * R*S*C/G multiply-adds per 4 bytes of traffic.  Widths 4..64 also run on
- * the tensor cores as block-diagonal implicit GEMMs: always in
- * conv2d_grouped_wgrad, and in the _ws variants of fprop and dgrad (width
- * 64 only there).  Every other G gives UNSUPPORTED.  Each output accumulates in fp32 over its taps
+ * R*S*C/G multiply-adds per 4 bytes of traffic.  The tensor cores run
+ * grouped layers as block-diagonal implicit GEMMs with 64-wide tiles of
+ * whole groups: always in conv2d_grouped_wgrad, and in the _ws variants of
+ * fprop and dgrad.  That covers C == K with widths 4 and up, and C != K
+ * (channel multipliers, K/G != C/G), whenever the per-group channel count
+ * on the tile side (K/G for fprop and wgrad, C/G for dgrad) divides 64 or
+ * is a multiple of 64, and the reduction window a tile reads from the
+ * other side is a multiple of 8 channels.  The window is 64 / (K/G) * (C/G)
+ * channels in the first case and C/G in the second (for dgrad swap C and
+ * K).  C and K must be multiples of 8.  Every other G gives UNSUPPORTED,
+ * and C != K only runs through the workspace entry points.  Each output accumulates in fp32 over its taps
  * in (r, s) order, group channels innermost (wgrad: over N*P*Q in a fixed
  * per-CTA order, then the CTAs' partial sums in a fixed order), so results
  * are deterministic.
@@ -305,12 +312,12 @@ IGCONV_API igconv_status_t conv2d_grouped_dgrad(const igconv_problem_t *prob, in
                                                 float alpha, float beta, void *stream);
 
 /* Grouped fprop with a caller-owned workspace, which opens the tensor-core
- * path: for C == K and a group width C/G of 4, 8, 16, 32 or 64 the
- * convolution runs as an implicit GEMM over 64-channel blocks in which
- * output channels 64n .. 64n + 63 reduce over input block n only, against a
- * block-diagonal copy of the filter that the call writes into the workspace
- * ([K][R][S][64], zeros outside each output channel's group).  Every other
- * G is exactly conv2d_grouped_fprop (the workspace is not used).  Same
+ * path (the coverage above): the convolution runs as an implicit GEMM in
+ * which output channels 64n .. 64n + 63 (whole groups) reduce only over the
+ * input channels their groups read, against a dense block-diagonal copy of
+ * the filter that the call writes into the workspace ([K][R][S][C], zeros
+ * outside each output channel's group; K*R*S*C*2 bytes).  Every other G is
+ * exactly conv2d_grouped_fprop (the workspace is not used).  Same
  * result definition, arguments and errors as conv2d_grouped_fprop, plus
  *   workspace  device memory of at least
  *              conv2d_grouped_fprop_workspace_size() bytes, caller-owned,
@@ -326,12 +333,13 @@ IGCONV_API igconv_status_t conv2d_grouped_fprop_ws(const igconv_problem_t *prob,
                                                    float beta, int relu, void *workspace,
                                                    size_t workspace_bytes, void *stream);
 
-/* Grouped dgrad with a caller-owned workspace: for C == K and a group width
- * of 4, 8, 16, 32 or 64 the dgrad implicit GEMM (with its residue classes
- * for strides) runs on the tensor cores with 64-wide tiles in which dX
- * channels 64n .. 64n + 63 reduce over dY channel block n only, against the
- * block-diagonal filter image the call writes into the workspace (as in
- * conv2d_grouped_fprop_ws).  Every other G is exactly conv2d_grouped_dgrad.
+/* Grouped dgrad with a caller-owned workspace: within the tensor-core
+ * coverage above (tiles over C) the dgrad implicit GEMM (with its residue
+ * classes for strides) runs with 64-wide tiles in which dX channels
+ * 64n .. 64n + 63 (whole groups) reduce only over the dY channels of their
+ * groups, against the dense block-diagonal filter image the call writes into
+ * the workspace (as in conv2d_grouped_fprop_ws).  Every other G is exactly
+ * conv2d_grouped_dgrad.
  * Arguments and errors as conv2d_grouped_dgrad, plus the workspace (at
  * least conv2d_grouped_dgrad_workspace_size() bytes, caller-owned,
  * overwritten, not shared with a concurrent call; WORKSPACE if missing or
@@ -344,10 +352,10 @@ IGCONV_API igconv_status_t conv2d_grouped_dgrad_ws(const igconv_problem_t *prob,
                                                    float alpha, float beta, void *workspace,
                                                    size_t workspace_bytes, void *stream);
 
-/* Workspace bytes conv2d_grouped_wgrad needs (widths 1, 2: fp32 partial
- * sums [splits][R*S][C][C/G]; widths 4..64: the block-diagonal GEMM's
- * split partials and the fp32 gradient of the block-local filter
- * [K][R][S][64]); the split count follows the current device's SM count
+/* Workspace bytes conv2d_grouped_wgrad needs (the direct kernels, C == K
+ * widths 1 and 2: fp32 partial sums [splits][R*S][C][C/G]; the tensor-core
+ * path: the block-diagonal GEMM's split partials and the fp32 gradient of
+ * the windowed filter [K][R][S][window rounded up to 64]); the split count follows the current device's SM count
  * and the kernel's occupancy, which this call queries without enqueuing
  * work).  0 for an invalid or uncovered problem. */
 IGCONV_API size_t conv2d_grouped_wgrad_workspace_size(const igconv_problem_t *prob, int groups,

@@ -193,14 +193,26 @@ def test_grouped_reject_invalid(igc):
                                     None) == 1
     assert lib.conv2d_grouped_dgrad(ctypes.byref(pb), 16, igc.F16, A, B, None, Cp + 2, 1.0, 0.0,
                                     None) == 3
-    assert lib.conv2d_grouped_wgrad(ctypes.byref(pbk), 4, igc.F16, igc.F32, A, B, None, Cp, 1.0,
-                                    0.0, None, 0, None) == 2
+    # C != K whose 64-wide tiles would split a group (24 output channels per
+    # group): no path at all
+    pb_split = igc.Problem.make(_pb(C=24, K=48))
+    assert lib.conv2d_grouped_wgrad(ctypes.byref(pb_split), 2, igc.F16, igc.F32, A, B, None, Cp,
+                                    1.0, 0.0, None, 0, None) == 2
     assert lib.conv2d_grouped_wgrad(ctypes.byref(pb), 16, igc.F16, igc.I8, A, B, None, Cp, 1.0,
                                     0.0, None, 0, None) == 2
     assert igc.conv2d_grouped_wgrad_workspace_size(_pb(), 5, igc.F16, igc.F32) == 0
-    # tensor-core grouped fprop: workspace only for C == K and widths 4..64
+    # tensor-core grouped fprop: a workspace (the dense block-diagonal
+    # filter, K*R*S*C*2 bytes) for C == K from width 4 and for C != K when
+    # the tiles hold whole groups and the windows are multiples of 8
     assert igc.conv2d_grouped_fprop_workspace_size(_pb(C=128, K=128), 32, igc.BF16) >= \
+        128 * 9 * 128 * 2
+    assert igc.conv2d_grouped_fprop_workspace_size(_pb(C=64, K=128), 16, igc.BF16) >= \
         128 * 9 * 64 * 2
+    assert igc.conv2d_grouped_dgrad_workspace_size(_pb(C=128, K=64), 16, igc.BF16) >= \
+        64 * 9 * 128 * 2
+    assert igc.conv2d_grouped_fprop_workspace_size(_pb(C=24, K=48), 2, igc.BF16) == 0
+    # 16 output channels per group of 1 input channel: 4-channel windows
+    assert igc.conv2d_grouped_fprop_workspace_size(_pb(C=16, K=256), 16, igc.BF16) == 0
     assert igc.conv2d_grouped_fprop_workspace_size(_pb(C=128, K=128), 64, igc.BF16) == 0
     assert igc.conv2d_grouped_fprop_workspace_size(_pb(C=128, K=128), 2, igc.F32) == 0
     pb128 = igc.Problem.make(_pb(C=128, K=128))

@@ -205,7 +205,7 @@ def run_fprop_ws(pb, inp, fmt, G, bias=False, alpha=1.0, beta=0.0, relu=False):
     P, Q = igc.conv2d_output_size(pb)
     Y, check = guarded_empty((pb["N"], P, Q, pb["K"]), FMT[fmt], "cuda")
     need = igc.conv2d_grouped_fprop_workspace_size(pb, G, FMT[fmt])
-    assert need >= pb["K"] * pb["R"] * pb["S"] * 64 * 2
+    assert need >= pb["K"] * pb["R"] * pb["S"] * pb["C"] * 2  # the block-diagonal filter
     ws = torch.empty(need, dtype=torch.uint8, device="cuda")
     igc.conv2d_grouped_fprop_ws(pb, G, FMT[fmt], inp["X"].cuda(), inp["W"].cuda(),
                                 inp["bias"].cuda() if bias else None,
@@ -232,7 +232,7 @@ def test_grouped_tensor_core_fprop_integer_exact(case):
 def run_dgrad_ws(pb, inp, fmt, G, alpha=1.0, beta=0.0):
     dX, check = guarded_empty((pb["N"], pb["H"], pb["W"], pb["C"]), FMT[fmt], "cuda")
     need = igc.conv2d_grouped_dgrad_workspace_size(pb, G, FMT[fmt])
-    assert need >= pb["K"] * pb["R"] * pb["S"] * 64 * 2
+    assert need >= pb["K"] * pb["R"] * pb["S"] * pb["C"] * 2
     ws = torch.empty(need, dtype=torch.uint8, device="cuda")
     igc.conv2d_grouped_dgrad_ws(pb, G, FMT[fmt], inp["dY"].cuda(), inp["W"].cuda(),
                                 inp["C_dgrad"].cuda() if beta != 0.0 else None, dX, alpha, beta,
@@ -282,6 +282,62 @@ def test_grouped_tensor_core_fprop_random_normal(case):
     assert_close(got, ref, A, "bf16", "grouped tensor-core fprop")
 
 
+# (problem, groups) with C != K (and one C == K width above 64): a 64-wide
+# tile holds whole groups and reduces over its window of the other side's
+# channels (fprop / wgrad tiles over K, dgrad tiles over C)
+GROUPED_CK = [
+    (problem(2, 10, 11, 64, 128, 3, 3, (1, 1)), 16),                  # 4 -> 8 per group
+    (problem(1, 12, 9, 128, 64, 3, 3, (1, 1), (2, 2)), 16),           # 8 -> 4, stride 2
+    (problem(2, 9, 10, 32, 64, 3, 3, (1, 1)), 32),                    # depthwise x2 multiplier
+    (problem(1, 8, 9, 64, 256, 1, 1), 2),                             # 32 -> 128: two tiles a group
+    (problem(1, 9, 8, 256, 64, 3, 3, (1, 1)), 4),                     # 64 -> 16: 4-block windows
+    (problem(1, 8, 8, 256, 256, 3, 3, (1, 1)), 2),                    # C == K, width 128
+    (problem(1, 10, 10, 48, 96, 3, 3, (2, 2), (1, 1), (2, 2)), 6),    # ragged tiles, dilation 2
+]
+
+
+@pytest.mark.parametrize("case", GROUPED_CK, ids=_gid)
+def test_grouped_channel_ratio_integer_exact(case):
+    """fprop (bias, ReLU, alpha / beta), dgrad and wgrad of grouped layers
+    with C != K on the tensor cores, bit-exact against the oracle."""
+    pb, G = case
+    inp, P, Q = inputs(pb, "f16", "int_uniform", 48, bias=True, cin=True, dw_dtype="f32",
+                       groups=G)
+    X, Wt, dY = f64(inp["X"]), f64(inp["W"]), f64(inp["dY"])
+    for bias, relu, alpha, beta in [(True, True, 1.0, 0.0), (False, False, 2.0, -1.0)]:
+        got = run_fprop_ws(pb, inp, "f16", G, bias=bias, relu=relu, alpha=alpha, beta=beta)
+        ref = oracle.grouped_fprop(pb, G, X, Wt, bias=f64(inp["bias"]) if bias else None,
+                                   relu=relu, Cin=f64(inp["C_fprop"]) if beta else None,
+                                   alpha=alpha, beta=beta)
+        assert_exact(got, ref, "f16", f"grouped C != K fprop relu={relu} beta={beta}")
+    for alpha, beta in [(1.0, 0.0), (0.5, 2.0)]:
+        got = run_dgrad_ws(pb, inp, "f16", G, alpha, beta)
+        ref = oracle.grouped_dgrad(pb, G, dY, Wt, Cin=f64(inp["C_dgrad"]) if beta else None,
+                                   alpha=alpha, beta=beta)
+        assert_exact(got, ref, "f16", f"grouped C != K dgrad beta={beta}")
+    for alpha, beta in [(1.0, 0.0), (0.5, 2.0)]:
+        got = run_wgrad(pb, inp, "f16", "f32", alpha, beta, G=G)
+        ref = oracle.grouped_wgrad(pb, G, X, dY, Cin=f64(inp["C_wgrad"]) if beta else None,
+                                   alpha=alpha, beta=beta)
+        assert_exact(got, ref, "f32", f"grouped C != K wgrad beta={beta}")
+
+
+@pytest.mark.parametrize("case", [GROUPED_CK[0], GROUPED_CK[4]], ids=_gid)
+def test_grouped_channel_ratio_random_normal(case):
+    pb, G = case
+    inp, P, Q = inputs(pb, "bf16", "normal_he", 49, bias=True, dw_dtype="f32", groups=G)
+    X, Wt, dY = f64(inp["X"]), f64(inp["W"]), f64(inp["dY"])
+    got = run_fprop_ws(pb, inp, "bf16", G, bias=True, relu=True)
+    ref, A = oracle.grouped_fprop(pb, G, X, Wt, bias=f64(inp["bias"]), relu=True, want_abs=True)
+    assert_close(got, ref, A, "bf16", "grouped C != K fprop")
+    got = run_dgrad_ws(pb, inp, "bf16", G)
+    ref, A = oracle.grouped_dgrad(pb, G, dY, Wt, want_abs=True)
+    assert_close(got, ref, A, "bf16", "grouped C != K dgrad")
+    got = run_wgrad(pb, inp, "bf16", "f32", G=G)
+    ref, A = oracle.grouped_wgrad(pb, G, X, dY, want_abs=True)
+    assert_close(got, ref, A, "f32", "grouped C != K wgrad")
+
+
 def test_grouped_ws_falls_back_to_direct_kernels():
     """Widths without a tensor-core path (depthwise, 2) take the direct
     kernel through the _ws entry point: identical bits."""
@@ -313,7 +369,8 @@ def test_groups_one_is_the_dense_path():
 
 def test_uncovered_groups_are_unsupported():
     # group width 64 has no direct kernel (only the workspace entry point's
-    # tensor-core path), and C != K with groups > 1 has neither
+    # tensor-core path); C != K has only the tensor-core path, and only when
+    # a 64-wide tile holds whole groups (24 output channels per group: no)
     pb = problem(1, 8, 8, 128, 128, 3, 3, (1, 1))
     X = torch.zeros((1, 8, 8, 128), dtype=torch.bfloat16, device="cuda")
     Wt = torch.zeros((128, 3, 3, 64), dtype=torch.bfloat16, device="cuda")
@@ -321,12 +378,14 @@ def test_uncovered_groups_are_unsupported():
     with pytest.raises(igc.IgconvError) as e:
         igc.conv2d_grouped_fprop(pb, 2, torch.bfloat16, X, Wt, None, None, Y)
     assert e.value.status == 2
-    pb = problem(1, 8, 8, 16, 32, 3, 3, (1, 1))
-    X = torch.zeros((1, 8, 8, 16), dtype=torch.bfloat16, device="cuda")
-    Wt = torch.zeros((32, 3, 3, 8), dtype=torch.bfloat16, device="cuda")
+    pb = problem(1, 8, 8, 24, 48, 3, 3, (1, 1))
+    assert igc.conv2d_grouped_fprop_workspace_size(pb, 2, torch.bfloat16) == 0
+    X = torch.zeros((1, 8, 8, 24), dtype=torch.bfloat16, device="cuda")
+    Wt = torch.zeros((48, 3, 3, 12), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(igc.IgconvError) as e:
         igc.grouped_fprop(pb, 2, X, Wt)
     assert e.value.status == 2
+    device_ok()
 
 
 @pytest.mark.parametrize("name", GROUPED_SWEEP)
