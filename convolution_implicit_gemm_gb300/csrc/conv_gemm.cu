@@ -102,6 +102,7 @@ struct Sched {
   int conv;  // operands are the convolution's (fprop / dgrad), not wgrad's
   int pair;  // CTA pairs: a unit is 256 rows, this CTA takes the half of its rank
   int rank;  // this CTA's rank in its pair (0 without pairs)
+  int raster;  // fprop / dgrad tile order (ConvGemmParams::raster)
 };
 
 template <bool PAIR>
@@ -118,7 +119,29 @@ __device__ __forceinline__ Sched load_sched(const ConvGemmParams& p) {
   s.cblocks = p.cblocks;
   s.pair = PAIR ? 1 : 0;  // the host sets p.pair for the PAIR kernels only
   s.rank = PAIR ? static_cast<int>(cluster_ctarank() & 1u) : 0;
+  s.raster = p.raster;
   return s;
+}
+
+// Tile (row um, column tn) of local unit index t in a grid of tm x tn_count
+// tiles.  g <= 1: columns fastest (all column tiles of a row tile run at
+// about the same time, so its A rows are read from L2 once per wave); g > 1:
+// the grid is cut into runs of g row tiles, and within a run the rows are
+// walked fastest, column by column, so that a wave of CTAs covers a compact
+// block of rows x columns (the swizzled order of CUTLASS's threadblock
+// swizzle).
+__device__ __forceinline__ void raster_tile(int t, int tm, int tn_count, int g, int* um, int* tn) {
+  if (g <= 1) {
+    *um = t / tn_count;
+    *tn = t - *um * tn_count;
+    return;
+  }
+  const int run = t / (g * tn_count);
+  const int r = t - run * g * tn_count;
+  const int left = tm - run * g;
+  const int rows = left < g ? left : g;
+  *tn = r / rows;
+  *um = run * g + (r - *tn * rows);
 }
 
 // The units of this CTA (pair) are first, first + stride, ...
@@ -145,9 +168,10 @@ __device__ __forceinline__ Work decode_unit(const ConvGemmParams& p, const Sched
     while (i + 1 < sc.nsub && u >= p.sub[i + 1].tile_begin) ++i;
     w.sub = i;
     const int local = u - p.sub[i].tile_begin;
-    w.tile_m = local / sc.tiles_n;
-    w.tile_n = local - w.tile_m * sc.tiles_n;
-    if (sc.pair) w.tile_m = 2 * w.tile_m + sc.rank;  // pairs: one sub-problem only
+    // pairs (one sub-problem only): a unit row is two 128-row tiles
+    const int unit_rows = sc.pair ? (p.sub[i].tiles_m + 1) / 2 : p.sub[i].tiles_m;
+    raster_tile(local, unit_rows, sc.tiles_n, sc.raster, &w.tile_m, &w.tile_n);
+    if (sc.pair) w.tile_m = 2 * w.tile_m + sc.rank;
     w.split = 0;
     w.kb0 = 0;
     w.kb1 = p.sub[i].rcount * p.sub[i].scount * sc.cblocks;
@@ -172,7 +196,7 @@ __device__ __forceinline__ void walk_begin(const ConvGemmParams& p, const Sched&
                                            UnitWalk& it) {
   it.u = unit_first(sc);
   it.stride = unit_stride(sc);
-  it.fast = sc.epi != EPI_PARTIAL && sc.nsub == 1;
+  it.fast = sc.epi != EPI_PARTIAL && sc.nsub == 1 && sc.raster <= 1;
   it.tm = it.tn = it.gq = it.gr = it.nk = 0;
   it.mstep = sc.pair ? 2 : 1;
   if (it.fast) {

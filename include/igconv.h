@@ -576,6 +576,12 @@ IGCONV_API const char *igconv_status_string(igconv_status_t status);
  *                             * C <= 64, else the tap-packed one); 1 always
  *                             the tap-packed path.  Query workspace sizes
  *                             after setting it.
+ *   IGCONV_TUNE_RASTER        order in which the persistent CTAs take the
+ *                             fprop / dgrad tiles (the "Swizzling Stride"
+ *                             of the CUTLASS example): 0 or 1 column tiles
+ *                             fastest (the built-in order); g in 2..64 runs
+ *                             of g row tiles, rows fastest within each
+ *                             column.  Results are bit-identical.
  * Returns INVALID_ARG for an unknown key or value. */
 typedef enum {
     IGCONV_TUNE_WGRAD_SPLITS = 1,
@@ -584,7 +590,8 @@ typedef enum {
     IGCONV_TUNE_CTA_PAIRS = 4,
     IGCONV_TUNE_EPI_GROUPS = 5,
     IGCONV_TUNE_CONV_SPLITS = 6,
-    IGCONV_TUNE_FEW_CHANNELS = 7
+    IGCONV_TUNE_FEW_CHANNELS = 7,
+    IGCONV_TUNE_RASTER = 8
 } igconv_tune_key_t;
 IGCONV_API igconv_status_t igconv_set_tuning(igconv_tune_key_t key, int value);
 

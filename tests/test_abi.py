@@ -166,6 +166,10 @@ def test_tuning_keys(igc):
     assert lib.igconv_set_tuning(igc.TUNE_FEW_CHANNELS, 2) == 1
     assert lib.igconv_set_tuning(igc.TUNE_FEW_CHANNELS, 1) == 0
     assert lib.igconv_set_tuning(igc.TUNE_FEW_CHANNELS, 0) == 0
+    assert lib.igconv_set_tuning(igc.TUNE_RASTER, 65) == 1
+    assert lib.igconv_set_tuning(igc.TUNE_RASTER, -1) == 1
+    assert lib.igconv_set_tuning(igc.TUNE_RASTER, 8) == 0
+    assert lib.igconv_set_tuning(igc.TUNE_RASTER, 0) == 0
 
 
 def test_grouped_reject_invalid(igc):
