@@ -250,11 +250,17 @@ class Layer:
         self.d2h = sum(t.numel() * t.element_size() for t in outs)
 
     def copy_in(self):
-        self.X.copy_(self.hX, non_blocking=True)
-        self.W.copy_(self.hW, non_blocking=True)
-        self.dY.copy_(self.hdY, non_blocking=True)
-        if self.bias:
-            self.b.copy_(self.hb, non_blocking=True)
+        for copy in self.copy_in_parts():
+            copy()
+
+    def copy_in_parts(self):
+        """fprop's inputs (X, W, bias), then dY (dgrad and wgrad)."""
+        def fwd():
+            self.X.copy_(self.hX, non_blocking=True)
+            self.W.copy_(self.hW, non_blocking=True)
+            if self.bias:
+                self.b.copy_(self.hb, non_blocking=True)
+        return fwd, lambda: self.dY.copy_(self.hdY, non_blocking=True)
 
     def compute(self):
         self.fprop()
@@ -262,41 +268,62 @@ class Layer:
         self.wgrad()
 
     def copy_out(self):
-        self.hY.copy_(self.Y, non_blocking=True)
-        self.hdX.copy_(self.dX, non_blocking=True)
-        self.hdW.copy_(self.dW, non_blocking=True)
+        for copy in self.copy_out_parts():
+            copy()
+
+    def copy_out_parts(self):
+        """The three result copies, in pass order (Y, dX, dW)."""
+        return (lambda: self.hY.copy_(self.Y, non_blocking=True),
+                lambda: self.hdX.copy_(self.dX, non_blocking=True),
+                lambda: self.hdW.copy_(self.dW, non_blocking=True))
 
 
 class E2EPipeline:
     """One end-to-end step through the C ABI with host buffers: every layer's
-    inputs copied from pinned host memory on one stream, its three passes
-    on a second stream once its inputs have landed, its outputs copied back
-    on a third once they are computed.  Layer i's passes overlap layer
-    i+1's input copy and layer i-1's output copy, and the two copy
-    directions run at the same time.  The step starts and ends on `main`,
-    so consecutive steps never overlap."""
+    inputs copied from pinned host memory on one stream (X and W before dY,
+    so fprop can start first), its three passes on a second stream once
+    their own inputs have landed, and each pass's result
+    copied back on a third as soon as that pass is done (Y after fprop, dX
+    after dgrad, dW after wgrad).  The two copy directions run at the same
+    time (the host link carries ~210 GB/s in, ~190 out, ~336 together), so
+    the step's floor is its bytes over the combined rate plus the first
+    layer's input copy and the last layer's output copy, which nothing
+    overlaps: the layers are taken smallest input first and smallest output
+    last.  The step starts and ends on `main`, so consecutive steps never
+    overlap."""
 
     def __init__(self, layers, main):
-        self.layers, self.main = layers, main
+        rest = list(layers)
+        first = min(rest, key=lambda L: L.h2d)
+        rest.remove(first)
+        last = min(rest, key=lambda L: L.d2h) if rest else None
+        if last is not None:
+            rest.remove(last)
+        self.layers = [first] + rest + ([last] if last is not None else [])
+        self.main = main
         self.s_in, self.s_c, self.s_out = (torch.cuda.Stream() for _ in range(3))
-        self.ev_in = [torch.cuda.Event() for _ in layers]
-        self.ev_c = [torch.cuda.Event() for _ in layers]
+        self.ev_in = [[torch.cuda.Event() for _ in range(2)] for _ in self.layers]
+        self.ev_pass = [[torch.cuda.Event() for _ in range(3)] for _ in self.layers]
 
     def step(self):
         for st in (self.s_in, self.s_c, self.s_out):
             st.wait_stream(self.main)
         with torch.cuda.stream(self.s_in):
-            for L, ev in zip(self.layers, self.ev_in):
-                L.copy_in()
-                ev.record(self.s_in)
-        for L, ei, ec in zip(self.layers, self.ev_in, self.ev_c):
-            self.s_c.wait_event(ei)
-            with torch.cuda.stream(self.s_c):
-                L.compute()
-                ec.record(self.s_c)
-            self.s_out.wait_event(ec)
-            with torch.cuda.stream(self.s_out):
-                L.copy_out()
+            for L, evs in zip(self.layers, self.ev_in):
+                for copy, ev in zip(L.copy_in_parts(), evs):
+                    copy()
+                    ev.record(self.s_in)
+        for L, ei, evs in zip(self.layers, self.ev_in, self.ev_pass):
+            # fprop needs X and W only; dgrad and wgrad also dY
+            for run, need, ev in zip((L.fprop, L.dgrad, L.wgrad), (ei[0], ei[1], ei[1]), evs):
+                self.s_c.wait_event(need)
+                with torch.cuda.stream(self.s_c):
+                    run()
+                    ev.record(self.s_c)
+            for copy, ev in zip(L.copy_out_parts(), evs):
+                self.s_out.wait_event(ev)
+                with torch.cuda.stream(self.s_out):
+                    copy()
         self.main.wait_stream(self.s_in)
         self.main.wait_stream(self.s_c)
         self.main.wait_stream(self.s_out)
@@ -623,9 +650,11 @@ def run_ours(args, rank, world, local_rank):
                "d2h_bytes_per_step": sum(L.d2h for L in layers),
                "ms_per_step": e2e_ms, "steps": len(e2e_all),
                "ms_min_max": [min(e2e_all), max(e2e_all)],
-               "how": "per layer: pinned H2D copies on one stream, the three passes on a "
-                      "second once the inputs landed, D2H copies of Y, dX, dW on a third; "
-                      "layers overlap, steps do not"}
+               "how": "per layer: pinned H2D copies on one stream (X, W, then dY), each pass "
+                      "on a second once its inputs landed, each result's D2H copy on a third as "
+                      "soon as its pass is done; layers overlap (smallest input first, "
+                      "smallest output last), steps do not",
+               "layer_order": [L.name for L in pipe.layers]}
 
     rows = None
     if not args.no_rows and rank == 0:
