@@ -437,6 +437,34 @@ igconv_problem_t few_pack_problem(const igconv_problem_t* pb, const FewPack& f) 
   return v;
 }
 
+// Few-channel dgrad on the same space-to-depth image but without windows:
+// one packed pixel per column (ppr = 1, cz = the used channels rounded up to
+// a multiple of 8), so the problem is a stride-1 convolution over cz
+// channels with R2 x S2 taps whose data gradient is the gradient of the
+// packed image; every X element was copied to exactly one packed element,
+// so dX is a gather of it.  Eligibility as few_pack_plan.
+bool few_pack_plan_dgrad(const igconv_problem_t* pb, int P, int Q, FewPack* f) {
+  if (!few_pack_plan(pb, P, Q, f)) return false;
+  const int used = f->fh * f->fw * f->C;
+  f->cz = (used + 7) / 8 * 8;
+  f->ppr = 1;
+  f->Sv = floor_div(pb->S - 1 - pb->pad_w, f->fw) - f->B0 + 1;
+  f->Wv = Q + f->Sv - 1;
+  f->Wz = f->Wv;
+  return true;
+}
+
+struct FewDgradPackWs {
+  size_t w_bytes, z_bytes, total;
+};
+FewDgradPackWs few_dgrad_pack_ws(const igconv_problem_t* pb, const FewPack& f) {
+  FewDgradPackWs w;
+  w.w_bytes = round256(static_cast<size_t>(pb->K) * f.R2 * f.Sv * f.cz * 2);
+  w.z_bytes = round256(static_cast<size_t>(pb->N) * f.Hz * f.Wz * f.cz * sizeof(float));
+  w.total = w.w_bytes + w.z_bytes;
+  return w;
+}
+
 struct FewPackWs {
   size_t z_bytes, w_bytes;
   cuuint64_t strides[3];  // pixel, row, image strides of the packed image
@@ -1398,7 +1426,7 @@ igconv_status_t conv2d_fprop_ws(const igconv_problem_t* prob, igconv_dtype_t dty
     void* Zp = ws;
     void* Wpk = ws + pw.z_bytes;
     if (launch_few_pack_x(X, Zp, fpk, prob->N, prob->H, prob->W, cs) != cudaSuccess ||
-        launch_few_pack_filter(Wt, Wpk, fpk, prob->K, cs) != cudaSuccess)
+        launch_few_pack_filter(Wt, Wpk, fpk, prob->K, 64, cs) != cudaSuccess)
       return IGCONV_ERR_CUDA;
     if ((st = plan_fprop(p, bn, &vp, P, Q, bf16, Zp, Wpk, pw.strides)) != IGCONV_OK) return st;
     gW = Wpk;
@@ -1494,7 +1522,11 @@ size_t conv2d_dgrad_workspace_size(const igconv_problem_t* prob, igconv_dtype_t 
   int P = 0, Q = 0;
   if (check_shape(prob, &P, &Q) != IGCONV_OK) return 0;
   if (dtype != IGCONV_F16 && dtype != IGCONV_BF16) return 0;
-  if (prob->C < 8) return few_dgrad_ws(prob).total;
+  if (prob->C < 8) {
+    FewPack f;
+    if (few_pack_plan_dgrad(prob, P, Q, &f)) return few_dgrad_pack_ws(prob, f).total;
+    return few_dgrad_ws(prob).total;
+  }
   if (prob->stride_h != 1 || prob->stride_w != 1) return 0;
   const int sms = current_sm_count();
   const long long tiles_m = ceil_div(static_cast<long long>(prob->N) * prob->H * prob->W, kBlockM);
@@ -1518,10 +1550,60 @@ igconv_status_t conv2d_dgrad_ws(const igconv_problem_t* prob, igconv_dtype_t dty
   if (!dY || !Wt || !dX || (beta != 0.0f && !Cin)) return IGCONV_ERR_INVALID_ARG;
   if (!std::isfinite(alpha) || !std::isfinite(beta)) return IGCONV_ERR_INVALID_ARG;
   if (dtype != IGCONV_F16 && dtype != IGCONV_BF16) return IGCONV_ERR_UNSUPPORTED;
+  FewPack fdp{};
+  if (prob->C < 8 && few_pack_plan_dgrad(prob, P, Q, &fdp)) {
+    // few input channels at dilation 1: the dgrad of the stride-1 packed
+    // problem (filter repacked to [K][R2][S2][cz]) written as alpha * acc in
+    // fp32, then each X element's gradient gathered from its packed position
+    // and finished with beta * Cin and the cast
+    igconv_problem_t vd = *prob;
+    vd.H = fdp.Hz;
+    vd.W = fdp.Wz;
+    vd.C = fdp.cz;
+    vd.R = fdp.R2;
+    vd.S = fdp.Sv;
+    vd.pad_h = vd.pad_w = 0;
+    vd.stride_h = vd.stride_w = 1;
+    vd.dil_h = vd.dil_w = 1;
+    if ((st = check_limits(&vd, P, Q, 8)) != IGCONV_OK) return st;
+    if (!aligned16(dY) || (reinterpret_cast<uintptr_t>(Wt) & 1) ||
+        (reinterpret_cast<uintptr_t>(dX) & 1) ||
+        (beta != 0.0f && (reinterpret_cast<uintptr_t>(Cin) & 1)) ||
+        (workspace && !aligned16(workspace)))
+      return IGCONV_ERR_MISALIGNED;
+    const FewDgradPackWs fw = few_dgrad_pack_ws(prob, fdp);
+    if (!workspace || workspace_bytes < fw.total) return IGCONV_ERR_WORKSPACE;
+    DeviceState* dev = nullptr;
+    if ((st = device_state(&dev)) != IGCONV_OK) return st;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    void* Wz = ws;
+    float* dz = reinterpret_cast<float*>(ws + fw.w_bytes);
+    const int bf16 = dtype == IGCONV_BF16 ? 1 : 0;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (launch_few_pack_filter(Wt, Wz, fdp, prob->K, fdp.cz, cs) != cudaSuccess)
+      return IGCONV_ERR_CUDA;
+    ConvGemmParams p;
+    init_common(p, dev);
+    int bn = 0;
+    if ((st = plan_dgrad(p, &bn, &vd, P, Q, bf16, dY, Wz, dev->sm_count)) != IGCONV_OK) return st;
+    p.epi = EPI_STORE;
+    p.out_f32 = 1;
+    p.out = dz;
+    p.use_tma_store = 0;
+    p.alpha = alpha;
+    p.out_bf16 = bf16;
+    p.pf_base = Wz;
+    p.pf_bytes = static_cast<long long>(prob->K) * fdp.R2 * fdp.Sv * fdp.cz * 2;
+    if (p.units > 0 && launch_conv_gemm(p, bn, grid_for(p.units, dev), cs) != cudaSuccess)
+      return IGCONV_ERR_CUDA;
+    return from_cuda(launch_few_unpack_dx(dz, dX, fdp, prob->N, prob->H, prob->W, bf16,
+                                          beta != 0.0f ? Cin : nullptr, beta, cs));
+  }
   if (prob->C < 8) {
-    // few input channels: the dense dgrad over the filter padded to 8
-    // channels, alpha * acc written as fp32 rows of 8 channels, then the C
-    // real channels finished with beta * Cin and the cast
+    // few input channels (with dilation, or the tap-packed knob): the dense
+    // dgrad over the filter padded to 8 channels, alpha * acc written as fp32
+    // rows of 8 channels, then the C real channels finished with beta * Cin
+    // and the cast
     igconv_problem_t k8 = *prob;
     k8.C = 8;
     if ((st = check_limits(&k8, P, Q, 8)) != IGCONV_OK) return st;

@@ -862,8 +862,12 @@ cudaError_t launch_filter_taps8(const void* w, void* dst, int K, int RS, int C, 
 // one 8-element (16-byte) output vector per thread:
 //   few_pack_x:      X[N][H][W][C] -> Zp[N][Hz][Wz][cz] (space-to-depth by the
 //                    strides, zero padding stored)
-//   few_pack_filter: W[K][R][S][C] -> Wpk[K][R2 * Sv][64], each virtual
+//   few_pack_filter: W[K][R][S][C] -> Wpk[K][R2 * Sv][row], each virtual
 //                    channel the filter entry few_pack_decode names, or zero
+//                    (row = 64 for the windowed fprop; cz for the unwindowed
+//                    dgrad problem)
+//   few_unpack_dx:   the inverse gather for dgrad: each X element's gradient
+//                    is the one packed element it was copied to
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint4 pack8_u16(const uint16_t v[8]) {
   return make_uint4(v[0] | (static_cast<uint32_t>(v[1]) << 16),
@@ -907,13 +911,14 @@ __global__ void __launch_bounds__(256) few_pack_x_kernel(const uint16_t* __restr
 
 __global__ void __launch_bounds__(256) few_pack_filter_kernel(const uint16_t* __restrict__ Wt,
                                                               uint4* __restrict__ Wpk, FewPack f,
-                                                              long long total) {
+                                                              int row, long long total) {
   const int vts = f.R2 * f.Sv;
+  const int vpr = row / 8;  // output vectors per virtual tap
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    // i = (k * vts + vt) * 8 + v
-    const int v = static_cast<int>(i & 7);
-    const long long rest = i >> 3;
+    // i = (k * vts + vt) * vpr + v
+    const int v = static_cast<int>(i % vpr);
+    const long long rest = i / vpr;
     const int vt = static_cast<int>(rest % vts);
     const long long k = rest / vts;
     uint16_t o[8] = {0, 0, 0, 0, 0, 0, 0, 0};
@@ -924,6 +929,43 @@ __global__ void __launch_bounds__(256) few_pack_filter_kernel(const uint16_t* __
         o[t] = Wt[(k * f.R * f.S + tap) * f.C + c];
     }
     Wpk[i] = pack8_u16(o);
+  }
+}
+
+// dX[n][h][w][c] = cast(dz[n][zi][zj][e] + beta * Cin[n][h][w][c]) with
+// (zi, zj, e) the packed position X[n][h][w][c] was copied to: zi = h / fh -
+// A0, zj = w / fw - B0, e = ((h % fh) * fw + w % fw) * C + c; dz holds alpha
+// times the gradient of the packed image as fp32 [N][Hz][Wz][cz] (ppr = 1);
+// X elements outside the packed image's extent get 0 + beta * Cin.
+__global__ void __launch_bounds__(256) few_unpack_dx_kernel(const float* __restrict__ dz,
+                                                            uint16_t* __restrict__ dX, FewPack f,
+                                                            int H, int W, long long total,
+                                                            int out_bf16,
+                                                            const uint16_t* __restrict__ cin,
+                                                            float beta) {
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    // i = ((n * H + h) * W + w) * C + c
+    const int c = static_cast<int>(i % f.C);
+    long long rest = i / f.C;
+    const int w = static_cast<int>(rest % W);
+    rest /= W;
+    const int h = static_cast<int>(rest % H);
+    const long long n = rest / H;
+    const int zi = h / f.fh - f.A0, dy = h % f.fh;
+    const int zj = w / f.fw - f.B0, dx = w % f.fw;
+    const int e = (dy * f.fw + dx) * f.C + c;
+    // rows and columns past the packed image are read by no output (stride
+    // above the filter extent): their gradient is zero
+    float x = (zi < f.Hz && zj < f.Wz) ? dz[((n * f.Hz + zi) * f.Wz + zj) * f.cz + e] : 0.0f;
+    if (beta != 0.0f) {
+      const uint16_t u = cin[i];
+      const float cv = out_bf16 ? __uint_as_float(static_cast<uint32_t>(u) << 16)
+                                : __half2float(__ushort_as_half(u));
+      x = __fmaf_rn(beta, cv, x);
+    }
+    dX[i] = out_bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(x))
+                     : __half_as_ushort(__float2half_rn(x));
   }
 }
 
@@ -939,15 +981,29 @@ cudaError_t launch_few_pack_x(const void* X, void* Zp, const FewPack& f, int N, 
   return cudaGetLastError();
 }
 
-cudaError_t launch_few_pack_filter(const void* Wt, void* Wpk, const FewPack& f, int K,
+cudaError_t launch_few_pack_filter(const void* Wt, void* Wpk, const FewPack& f, int K, int row,
                                    cudaStream_t s) {
-  if (f.cz < 8 || f.cz > 64 || f.C < 1 || f.C > 8) return cudaErrorInvalidValue;
-  const long long total = static_cast<long long>(K) * f.R2 * f.Sv * 8;
+  if (f.cz < 8 || f.cz > 64 || f.C < 1 || f.C > 8 || row % 8 != 0 || row < 8 || row > 64)
+    return cudaErrorInvalidValue;
+  const long long total = static_cast<long long>(K) * f.R2 * f.Sv * (row / 8);
   long long blocks = (total + 255) / 256;
   if (blocks < 1) blocks = 1;
   if (blocks > 16384) blocks = 16384;
   few_pack_filter_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-      static_cast<const uint16_t*>(Wt), static_cast<uint4*>(Wpk), f, total);
+      static_cast<const uint16_t*>(Wt), static_cast<uint4*>(Wpk), f, row, total);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_few_unpack_dx(const float* dz, void* dX, const FewPack& f, int N, int H, int W,
+                                 int out_bf16, const void* cin, float beta, cudaStream_t s) {
+  if (f.C < 1 || f.C > 8 || f.fh < 1 || f.fw < 1) return cudaErrorInvalidValue;
+  const long long total = static_cast<long long>(N) * H * W * f.C;
+  long long blocks = (total + 255) / 256;
+  if (blocks < 1) blocks = 1;
+  if (blocks > 65536) blocks = 65536;
+  few_unpack_dx_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+      dz, static_cast<uint16_t*>(dX), f, H, W, total, out_bf16,
+      static_cast<const uint16_t*>(cin), beta);
   return cudaGetLastError();
 }
 

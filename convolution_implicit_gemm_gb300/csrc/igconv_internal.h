@@ -217,8 +217,10 @@ cudaError_t launch_filter_taps8(const void* w, void* dst, int K, int RS, int C, 
                                 cudaStream_t s);
 cudaError_t launch_few_pack_x(const void* X, void* Zp, const FewPack& f, int N, int H, int W,
                               cudaStream_t s);
-cudaError_t launch_few_pack_filter(const void* Wt, void* Wpk, const FewPack& f, int K,
+cudaError_t launch_few_pack_filter(const void* Wt, void* Wpk, const FewPack& f, int K, int row,
                                    cudaStream_t s);
+cudaError_t launch_few_unpack_dx(const float* dz, void* dX, const FewPack& f, int N, int H, int W,
+                                 int out_bf16, const void* cin, float beta, cudaStream_t s);
 cudaError_t launch_group_filter_dense(const void* w, void* dst, int K, int RS, int C, int cg,
                                       int kg, cudaStream_t s);
 cudaError_t launch_group_extract(const float* src, void* dW, int dw_dtype, const void* cin,

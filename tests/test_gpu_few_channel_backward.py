@@ -2,10 +2,13 @@
 oracle: the first layer of a CNN, whose pixels are too narrow for a 16-byte
 TMA row.
 
-dgrad runs the dense data gradient over the filter padded to 8 channels,
-writes alpha * acc as fp32 rows of 8 channels in the workspace, and a second
-kernel finishes the C real channels (beta * Cin, the cast).  wgrad has two
-paths.  At dilation 1 (stride_h * stride_w * C <= 64) the pixels are packed
+dgrad has two paths.  At dilation 1 (stride_h * stride_w * C <= 64) it is
+the data gradient of the stride-1 problem over the space-to-depth packed
+image, one packed pixel per column, written as fp32; each X element's
+gradient is then gathered from the packed element it was copied to (beta *
+Cin, the cast).  Otherwise (or with IGCONV_TUNE_FEW_CHANNELS = 1) it is the
+dense data gradient over the filter padded to 8 channels, written as fp32
+rows of 8 channels and finished the same way.  wgrad has two paths.  At dilation 1 (stride_h * stride_w * C <= 64) the pixels are packed
 by space-to-depth into a padded image whose 128-byte windows of consecutive
 packed pixels form the reduction operand's rows.  Otherwise (or with
 IGCONV_TUNE_FEW_CHANNELS = 1) the pixels are copied to 8-channel rows and
@@ -88,7 +91,7 @@ def run_wgrad(pb, inp, dtype, dw_dtype, alpha=1.0, beta=0.0):
 
 
 @pytest.mark.parametrize("pb", SHAPES, ids=_id)
-def test_dgrad_integer_exact(pb):
+def test_dgrad_integer_exact(pb, few_mode):
     inp, P, Q = inputs(pb, "f16", "int_uniform", 131, cin=True)
     for alpha, beta in [(1.0, 0.0), (1.0, 2.0), (-2.0, 0.5)]:
         got = run_dgrad(pb, inp, "f16", alpha, beta)
