@@ -2552,12 +2552,52 @@ igconv_status_t conv3d_wgrad(const igconv_problem3d_t* prob, igconv_dtype_t dtyp
   return from_cuda(e);
 }
 
+// Tile width, accumulator groups and split count of the int8 fprop.  Each
+// TMEM accumulator sums at most 16 reduction blocks (1024 products of
+// magnitude <= 2^14: integers below 2^24, exact in fp32), NI issuers deal
+// the blocks round-robin, and two TMEM buffers of NI * groups accumulators
+// must fit in the 512 columns.  The tile width shrinks until a tile's whole
+// reduction fits; when not even 64-wide tiles hold it (R*S*C above 4096),
+// the reduction is cut into equal ranges of at most 64 blocks whose exact
+// int32 partial tiles an ordered reduction adds before the requantisation.
+struct Int8FpropPlan {
+  int bn, groups, splits, kb_unit;  // kb_unit: most blocks one unit reduces
+};
+Int8FpropPlan plan_int8_fprop(const igconv_problem_t* prob, int P, int Q, int sm_count) {
+  Int8FpropPlan ip;
+  const int kblocks = prob->R * prob->S * ceil_div(prob->C, kBlockK);
+  ip.bn = choose_block_n(prob->K, ceil_div(static_cast<long long>(prob->N) * P * Q, kBlockM),
+                         sm_count);
+  ip.splits = 1;
+  for (;;) {
+    const int ni = issuers_for(ip.bn);
+    ip.kb_unit = ceil_div(kblocks, ip.splits);
+    ip.groups = ceil_div(ceil_div(ip.kb_unit, ni), 16);
+    if (2 * ni * ip.groups * ip.bn <= 512) break;
+    if (ip.bn > 64) {
+      ip.bn >>= 1;
+      continue;
+    }
+    // 64-wide tiles: two issuers x two groups of 16 blocks = 64 blocks a unit
+    ip.splits = ceil_div(kblocks, 2 * 2 * 16);
+  }
+  return ip;
+}
+
+size_t int8_fprop_split_bytes(const igconv_problem_t* prob, int P, int Q, const Int8FpropPlan& ip) {
+  if (ip.splits < 2) return 0;
+  const long long tiles_m = ceil_div(static_cast<long long>(prob->N) * P * Q, kBlockM);
+  return round256(static_cast<size_t>(ip.splits) * tiles_m * kBlockM *
+                  ceil_div(prob->K, ip.bn) * ip.bn * sizeof(int32_t));
+}
+
 size_t conv2d_fprop_int8_workspace_size(const igconv_problem_t* prob) {
   int P = 0, Q = 0;
   if (check_shape(prob, &P, &Q) != IGCONV_OK) return 0;
   const size_t xb = static_cast<size_t>(prob->N) * prob->H * prob->W * prob->C * 2;
   const size_t wb = static_cast<size_t>(prob->K) * prob->R * prob->S * prob->C * 2;
-  return ((xb + 255) / 256) * 256 + ((wb + 255) / 256) * 256;
+  const Int8FpropPlan ip = plan_int8_fprop(prob, P, Q, current_sm_count());
+  return round256(xb) + round256(wb) + int8_fprop_split_bytes(prob, P, Q, ip);
 }
 
 igconv_status_t conv2d_fprop_int8(const igconv_problem_t* prob, const int8_t* X, const int8_t* Wt,
@@ -2573,7 +2613,6 @@ igconv_status_t conv2d_fprop_int8(const igconv_problem_t* prob, const int8_t* X,
     return IGCONV_ERR_INVALID_ARG;
   if ((st = check_limits(prob, P, Q, 16)) != IGCONV_OK) return st;
   const long long kg = static_cast<long long>(prob->R) * prob->S * prob->C;
-  if (kg > 4096) return IGCONV_ERR_UNSUPPORTED;
   if (!aligned16(X) || !aligned16(Wt) || !aligned16(Y) || (bias && !aligned16(bias)) ||
       (workspace && !aligned16(workspace)))
     return IGCONV_ERR_MISALIGNED;
@@ -2593,44 +2632,47 @@ igconv_status_t conv2d_fprop_int8(const igconv_problem_t* prob, const int8_t* X,
 
   ConvGemmParams p;
   init_common(p, dev);
-  // Exactness: each TMEM accumulator sums at most 16 reduction blocks
-  // (1024 products of magnitude <= 128*128 = 2^14), so every partial sum is
-  // an integer of magnitude <= 2^24, exact in fp32.  With NI issuers the
-  // blocks are dealt round-robin, and each issuer's share is cut into groups
-  // of at most 16; there are NI * groups accumulators.
-  const int kblocks = prob->R * prob->S * ceil_div(prob->C, kBlockK);
-  int bn = choose_block_n(prob->K, ceil_div(static_cast<long long>(prob->N) * P * Q, kBlockM),
-                          dev->sm_count);
-  int groups = 0;
-  for (;;) {
-    const int ni = issuers_for(bn);
-    groups = ceil_div(ceil_div(kblocks, ni), 16);
-    if (2 * ni * groups * bn <= 512) break;  // two TMEM buffers of ni*groups accumulators
-    if (bn == 64) return IGCONV_ERR_UNSUPPORTED;
-    bn >>= 1;
-  }
+  // Exactness: each TMEM accumulator sums at most 16 reduction blocks, so
+  // every partial sum is an integer of magnitude <= 2^24, exact in fp32
+  // (plan_int8_fprop); the accumulators are added as int32.
+  const Int8FpropPlan ip = plan_int8_fprop(prob, P, Q, dev->sm_count);
+  const int bn = ip.bn;
   if ((st = plan_fprop(p, bn, prob, P, Q, 0, Xh, Wh)) != IGCONV_OK) return st;
   const int ni = issuers_for(bn);
-  p.num_acc = ni * groups;
-  p.kb_per_acc = ceil_div(ceil_div(kblocks, ni), groups);
-  p.epi = EPI_INT8;
-  p.out = Y;
-  p.use_tma_store = encode_out_2d(&p.mapY, Y, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
-                                  static_cast<long long>(prob->N) * P * Q, prob->K, 32,
-                                  CU_TENSOR_MAP_SWIZZLE_32B) ? 1 : 0;
-  p.bias = bias;
-  p.bias_cached = bias != nullptr && prob->K * 4 <= kBiasCacheBytes ? 1 : 0;
+  p.num_acc = ni * ip.groups;
+  p.kb_per_acc = ceil_div(ceil_div(ip.kb_unit, ni), ip.groups);
   p.relu = relu ? 1 : 0;
   int ex = 0;
   const float fr = std::frexp(M, &ex);  // M = fr * 2^ex, fr in [0.5, 1)
   p.rq_mant = static_cast<uint32_t>(std::ldexp(fr, 24));
   p.rq_exp = ex - 24;
+  int* part = nullptr;
+  if (ip.splits > 1) {
+    // split reduction: exact int32 partial tiles, then bias, ReLU and the
+    // requantisation in the ordered split reduction
+    part = reinterpret_cast<int*>(static_cast<uint8_t*>(Wh) +
+                                  ((static_cast<size_t>(wcount) * 2 + 255) / 256) * 256);
+    set_conv_split(p, bn, ip.splits, part);
+    p.int_acc = 1;
+  } else {
+    p.epi = EPI_INT8;
+    p.out = Y;
+    p.use_tma_store = encode_out_2d(&p.mapY, Y, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
+                                    static_cast<long long>(prob->N) * P * Q, prob->K, 32,
+                                    CU_TENSOR_MAP_SWIZZLE_32B) ? 1 : 0;
+    p.bias = bias;
+    p.bias_cached = bias != nullptr && prob->K * 4 <= kBiasCacheBytes ? 1 : 0;
+  }
 
   cudaError_t e = launch_i8_to_f16(X, Xh, xcount, s);
   if (e != cudaSuccess) return IGCONV_ERR_CUDA;
   e = launch_i8_to_f16(Wt, Wh, wcount, s);
   if (e != cudaSuccess) return IGCONV_ERR_CUDA;
-  return from_cuda(launch_conv_gemm(p, bn, grid_for(p.units, dev), s));
+  e = launch_conv_gemm(p, bn, grid_for(p.units, dev), s);
+  if (e != cudaSuccess || part == nullptr) return from_cuda(e);
+  return from_cuda(launch_conv_splitk_reduce_i8(part, ip.splits, p.ws_split_stride, p.ws_ld,
+                                                static_cast<long long>(prob->N) * P * Q, prob->K,
+                                                Y, bias, p.rq_mant, p.rq_exp, p.relu, s));
 }
 
 // ---------------------------------------------------------------------------

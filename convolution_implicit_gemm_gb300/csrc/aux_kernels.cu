@@ -630,6 +630,62 @@ __global__ void __launch_bounds__(256) conv_splitk_reduce_kernel(
   }
 }
 
+// int8 fprop split-K reduction: the splits' exact int32 partial sums of one
+// output element added modulo 2^32 in split order (as one int32
+// accumulator would), then the bias, ReLU and the exact half-even
+// requantisation of the unsplit epilogue (requant_rne).  Four consecutive
+// channels per thread.
+__global__ void __launch_bounds__(256) conv_splitk_reduce_i8_kernel(
+    const int* __restrict__ ws, int splits, long long split_stride, int ws_ld, long long rows,
+    int cols, int8_t* __restrict__ out, const int32_t* __restrict__ bias, uint32_t mant, int sh,
+    long long half_m1, int mode, int relu) {
+  const int cq = cols / 4;
+  const long long total = rows * cq;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long m = i / cq;
+    const int c = static_cast<int>(i - m * cq) * 4;
+    uint32_t a[4] = {0u, 0u, 0u, 0u};
+    const int* src = ws + m * ws_ld + c;
+    for (int sp = 0; sp < splits; ++sp) {
+      const int4 v = *reinterpret_cast<const int4*>(src + sp * split_stride);
+      a[0] += static_cast<uint32_t>(v.x);
+      a[1] += static_cast<uint32_t>(v.y);
+      a[2] += static_cast<uint32_t>(v.z);
+      a[3] += static_cast<uint32_t>(v.w);
+    }
+    uint32_t packed = 0u;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      long long t = static_cast<long long>(static_cast<int>(a[j])) + (bias ? bias[c + j] : 0);
+      if (relu && t < 0) t = 0;
+      const int y = requant_rne(t, mant, sh, half_m1, mode);
+      packed |= (static_cast<uint32_t>(y) & 0xFFu) << (8 * j);
+    }
+    *reinterpret_cast<uint32_t*>(out + m * cols + c) = packed;
+  }
+}
+
+cudaError_t launch_conv_splitk_reduce_i8(const int* ws, int splits, long long split_stride,
+                                         int ws_ld, long long rows, int cols, int8_t* out,
+                                         const int32_t* bias, uint32_t rq_mant, int rq_exp,
+                                         int relu, cudaStream_t s) {
+  if (cols % 4 != 0 || ws_ld % 4 != 0 || split_stride % 4 != 0 || splits < 1)
+    return cudaErrorInvalidValue;
+  // M = mant * 2^rq_exp: the shift is -rq_exp, clamped as in the epilogue
+  const int sh_true = -rq_exp;
+  const int mode = sh_true < 1 ? 1 : (sh_true > 62 ? 2 : 0);
+  const int sh = sh_true < 1 ? 1 : (sh_true > 62 ? 62 : sh_true);
+  const long long half_m1 = (1LL << (sh - 1)) - 1;
+  const long long total = rows * (cols / 4);
+  long long blocks = (total + 255) / 256;
+  if (blocks < 1) blocks = 1;
+  if (blocks > 65536) blocks = 65536;
+  conv_splitk_reduce_i8_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+      ws, splits, split_stride, ws_ld, rows, cols, out, bias, rq_mant, sh, half_m1, mode, relu);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_conv_splitk_reduce(const float* ws, int splits, long long split_stride,
                                       int ws_ld, long long rows, int cols, void* out,
                                       int out_bf16, const void* cin, const void* bias,

@@ -766,25 +766,6 @@ __device__ __forceinline__ void unpack8(uint4 v, float (&f)[8], int bf16) {
   }
 }
 
-// round_half_even(t * M) clamped to int8 without branches, for M = mant *
-// 2^-sh and |t| < 2^33.  For 1 <= sh <= 62: with x = t * mant (exact in 64
-// bits) and b the lowest bit of floor(x / 2^sh), the quotient
-// floor((x + b + 2^(sh-1) - 1) / 2^sh) rounds x / 2^sh to nearest with ties to
-// the even neighbour (an arithmetic shift is the floor, also for negative x).
-// sh <= 0 means M >= 2^23, so every t != 0 saturates; sh >= 63 means M <
-// 2^-39, so |t * M| < 1/2 rounds to 0.  The caller passes sh clamped to
-// 1..62 and the mode of the true shift (0 in range, 1 saturate, 2 zero).
-__device__ __forceinline__ int requant_rne(long long t, uint32_t mant, int sh,
-                                          long long half_m1, int mode) {
-  const long long x = t * static_cast<long long>(mant);
-  const long long b = (x >> sh) & 1LL;
-  long long q = (x + b + half_m1) >> sh;
-  if (mode == 1) q = t > 0 ? 127 : (t < 0 ? -128 : 0);
-  if (mode == 2) q = 0;
-  q = q > 127 ? 127 : q;
-  q = q < -128 ? -128 : q;
-  return static_cast<int>(q);
-}
 
 // Writes 32 staged rows to global memory with coalesced 16-byte stores.
 // Each lane first puts its own row's n16 16-byte pieces in the warp's staging

@@ -191,6 +191,28 @@ __host__ __device__ inline bool few_pack_decode(const FewPack& f, int vt, int ev
   return true;
 }
 
+#ifdef __CUDACC__
+// round_half_even(t * M) clamped to int8 without branches, for M = mant *
+// 2^-sh and |t| < 2^33.  For 1 <= sh <= 62: with x = t * mant (exact in 64
+// bits) and b the lowest bit of floor(x / 2^sh), the quotient
+// floor((x + b + 2^(sh-1) - 1) / 2^sh) rounds x / 2^sh to nearest with ties to
+// the even neighbour (an arithmetic shift is the floor, also for negative x).
+// sh <= 0 means M >= 2^23, so every t != 0 saturates; sh >= 63 means M <
+// 2^-39, so |t * M| < 1/2 rounds to 0.  The caller passes sh clamped to
+// 1..62 and the mode of the true shift (0 in range, 1 saturate, 2 zero).
+__device__ __forceinline__ int requant_rne(long long t, uint32_t mant, int sh,
+                                          long long half_m1, int mode) {
+  const long long x = t * static_cast<long long>(mant);
+  const long long b = (x >> sh) & 1LL;
+  long long q = (x + b + half_m1) >> sh;
+  if (mode == 1) q = t > 0 ? 127 : (t < 0 ? -128 : 0);
+  if (mode == 2) q = 0;
+  q = q > 127 ? 127 : q;
+  q = q < -128 ? -128 : q;
+  return static_cast<int>(q);
+}
+#endif
+
 // Auxiliary kernels (aux_kernels.cu).
 cudaError_t launch_batched_transpose(const void* src, void* dst, long long batch, long long rows,
                                      long long cols, int elem_bytes, cudaStream_t s);
@@ -201,6 +223,12 @@ cudaError_t launch_wgrad_reduce(const float* ws, int splits, long long split_str
                                 int rows, int cols, int swapped, int K, int RS, int C, int cpad,
                                 void* dW, int dw_dtype, const void* cin, float alpha, float beta,
                                 cudaStream_t s, const FewPack* remap = nullptr);
+// int8 fprop split-K: y[m][k] = requant(relu(sum_s ws[s][m][k] + bias[k]))
+// with the int32 partials added modulo 2^32 in split order.
+cudaError_t launch_conv_splitk_reduce_i8(const int* ws, int splits, long long split_stride,
+                                         int ws_ld, long long rows, int cols, int8_t* out,
+                                         const int32_t* bias, uint32_t rq_mant, int rq_exp,
+                                         int relu, cudaStream_t s);
 cudaError_t launch_conv_splitk_reduce(const float* ws, int splits, long long split_stride,
                                       int ws_ld, long long rows, int cols, void* out,
                                       int out_bf16, const void* cin, const void* bias,

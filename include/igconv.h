@@ -459,7 +459,9 @@ IGCONV_API igconv_status_t conv2d_fprop_winograd(const igconv_problem_t *prob,
                                                  size_t workspace_bytes, void *stream);
 
 /* Bytes of device workspace conv2d_fprop_int8 needs (fp16 copies of X and
- * Wt, which the tensor cores consume).  Host only; 0 for an invalid problem. */
+ * Wt, which the tensor cores consume, and for R*S*C above 4096 the int32
+ * partial tiles of the split reduction).  Host only, queried on the current
+ * device; 0 for an invalid problem. */
 IGCONV_API size_t conv2d_fprop_int8_workspace_size(const igconv_problem_t *prob);
 
 /* Quantised forward pass.
@@ -477,7 +479,13 @@ IGCONV_API size_t conv2d_fprop_int8_workspace_size(const igconv_problem_t *prob)
  * half-even shift), so Y is unique.  Zero points are 0 (symmetric).
  *   X  [N][H][W][C] int8   Wt [K][R][S][C] int8   bias [K] int32 or NULL
  *   Y  [N][P][Q][K] int8 (written)
- *   scales finite and > 0.  C and K multiples of 16.  R*S*C <= 4096.
+ *   scales finite and > 0.  C and K multiples of 16.
+ * acc is exact while |acc| < 2^31.  Up to R*S*C = 4096 (64 blocks of 64
+ * channels) a tile's whole reduction fits its TMEM accumulators (at most
+ * 16 blocks each, so every fp32 partial sum is an exact integer).  Above
+ * that the reduction is split into equal ranges of at most 64 blocks whose
+ * int32 partial tiles are added in split order (modulo 2^32, as one int32
+ * accumulator would) before the bias, ReLU and requantisation.
  *   workspace  >= conv2d_fprop_int8_workspace_size() bytes, caller-owned,
  *              overwritten; not shared with a concurrent call.
  * Errors: INVALID_ARG, UNSUPPORTED, MISALIGNED, WORKSPACE, CUDA. */

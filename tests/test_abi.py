@@ -122,9 +122,11 @@ def test_dgrad_wgrad_int8_reject_invalid(igc):
     pb = igc.Problem.make(_pb(C=8))   # int8 needs multiples of 16
     assert lib.conv2d_fprop_int8(ctypes.byref(pb), A, B, None, Cp, 0.1, 0.1, 0.1, 1, None, 0,
                                  None) == 2
-    pb = igc.Problem.make(_pb(C=512, R=3, S=3))  # R*S*C > 4096
+    pb = igc.Problem.make(_pb(C=512, R=3, S=3))  # R*S*C > 4096: split, int32 partials
     assert lib.conv2d_fprop_int8(ctypes.byref(pb), A, B, None, Cp, 0.1, 0.1, 0.1, 1, None, 0,
-                                 None) == 2
+                                 None) == 4  # no workspace
+    assert igc.conv2d_fprop_int8_workspace_size(_pb(C=512, R=3, S=3)) > \
+        2 * 8 * 8 * 512 * 2 + 16 * 9 * 512 * 2
     pb = igc.Problem.make(_pb(C=32))
     assert lib.conv2d_fprop_int8(ctypes.byref(pb), A, B, None, Cp, 0.1, 0.1, 0.1, 1, None, 0,
                                  None) == 4  # no workspace

@@ -134,3 +134,47 @@ def test_int8_extreme_bias_is_exact():
     ref = oracle.fprop_int8(pb, inp["X"].numpy(), inp["W"].numpy(), bias.numpy(), 0.02, 0.01,
                             0.05, relu=False)
     np.testing.assert_array_equal(got, ref)
+
+
+# R*S*C above 4096: more reduction blocks than the TMEM accumulators of one
+# tile hold exactly, so the reduction is split into ranges of at most 64
+# blocks with exact int32 partial tiles, added in split order before the
+# bias, ReLU and requantisation
+SPLIT_SHAPES = [
+    problem(1, 7, 7, 512, 64, 3, 3, (1, 1)),          # 72 blocks: 2 splits (the 7x7 layer)
+    problem(2, 9, 8, 1024, 32, 3, 3, (1, 1)),         # 144 blocks: 3 splits
+    problem(1, 10, 10, 256, 48, 5, 5, (2, 2), (2, 2)),  # 100 blocks, stride 2
+    problem(1, 6, 7, 4112, 16, 1, 1),                 # 65 blocks, ragged channel block
+]
+
+
+@pytest.mark.parametrize("pb", SPLIT_SHAPES, ids=lambda p: "x".join(str(p[k]) for k in "NHWCKRS"))
+@pytest.mark.parametrize("relu", [True, False])
+def test_int8_split_reduction_exact(pb, relu):
+    P, Q = igc.conv2d_output_size(pb)
+    need = igc.conv2d_fprop_int8_workspace_size(pb)
+    fp16_copies = pb["N"] * pb["H"] * pb["W"] * pb["C"] * 2 + pb["K"] * pb["R"] * pb["S"] * pb["C"] * 2
+    assert need > fp16_copies  # the int32 partial tiles come on top
+    inp, P, Q = inputs(pb, "i8", "int8", 53, bias=True)
+    got = run_int8(pb, inp["X"], inp["W"], inp["bias"], 0.02, 0.01, 0.05, relu)
+    ref = oracle.fprop_int8(pb, inp["X"].numpy(), inp["W"].numpy(), inp["bias"].numpy(),
+                            0.02, 0.01, 0.05, relu=relu)
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_int8_split_worst_case_is_exact():
+    """9216 products of -128 * -127 (or * 127) per output over three splits:
+    |acc| = 149.8 M, every split's partial above 2^24.  With M = 1 and bias =
+    -acc + j the output is j only if partials and their sum are exact."""
+    K, C = 16, 1024
+    pb = problem(2, 3, 3, C, K, 3, 3)
+    X = torch.full((2, 3, 3, C), -128, dtype=torch.int8)
+    Wt = torch.empty((K, 3, 3, C), dtype=torch.int8)
+    for k in range(K):
+        Wt[k] = -127 if k % 2 == 0 else 127
+    acc = np.array([(1 if k % 2 == 0 else -1) * 9 * C * 128 * 127 for k in range(K)],
+                   dtype=np.int64)
+    j = np.arange(K, dtype=np.int64) - 8
+    bias = torch.from_numpy((-acc + j).astype(np.int32))
+    got = run_int8(pb, X, Wt, bias, 1.0, 1.0, 1.0, False)
+    np.testing.assert_array_equal(got.reshape(2, K), np.stack([j, j]).astype(np.int8))
