@@ -46,7 +46,8 @@ DeviceState g_dev[kMaxDevices];
 PFN_encodeTiled g_encode_tiled = nullptr;
 PFN_encodeIm2col g_encode_im2col = nullptr;
 std::atomic<int> g_tune_splits{0}, g_tune_bn{0}, g_tune_max_ctas{0}, g_tune_no_pairs{0},
-    g_tune_epi_groups{0}, g_tune_conv_splits{0}, g_tune_few_channels{0}, g_tune_raster{0};
+    g_tune_epi_groups{0}, g_tune_conv_splits{0}, g_tune_few_channels{0}, g_tune_raster{0},
+    g_tune_resident_b{0};
 
 igconv_status_t device_state(DeviceState** out) {
   int dev = 0;
@@ -322,6 +323,7 @@ void init_common(ConvGemmParams& p, const DeviceState* st) {
   p.splits = 1;
   p.epi_groups = g_tune_epi_groups.load();  // 0: the launcher decides
   p.raster = g_tune_raster.load();          // 0: column tiles fastest
+  p.res_b = g_tune_resident_b.load() == 1 ? 0 : 1;  // the launcher decides where it applies
 }
 
 // fprop plan (16-bit, or the int8 path's widened copies) on X [N,H,W,C],
@@ -1342,6 +1344,10 @@ igconv_status_t igconv_set_tuning(igconv_tune_key_t key, int value) {
     case IGCONV_TUNE_RASTER:
       if (value < 0 || value > 64) return IGCONV_ERR_INVALID_ARG;
       g_tune_raster.store(value);
+      return IGCONV_OK;
+    case IGCONV_TUNE_RESIDENT_FILTER:
+      if (value < 0 || value > 1) return IGCONV_ERR_INVALID_ARG;
+      g_tune_resident_b.store(value);
       return IGCONV_OK;
   }
   return IGCONV_ERR_INVALID_ARG;

@@ -65,14 +65,23 @@ constexpr int kStageWarpBytes = 2 * kStageBufBytes; // double-buffered per epilo
 constexpr int kBiasBytes = kBiasCacheBytes;  // bias vector cached in shared memory
 constexpr int kSmemLimit = 232448; // 227 KB: the most dynamic shared memory a CTA may use
 
-template <int BN, bool PAIR = false>
+// RESB: the filter stays resident in shared memory (loaded once per CTA,
+// up to kResBlocks reduction blocks of BN x 64), so a stage holds only the
+// A tile and the ring keeps all eight stages.  It pays only where the
+// per-tile work is short: with room for ten blocks (a 3x3 x 64 filter) the
+// ring shrank to six stages and the 64-wide 3x3 layers ran 20 % slower.
+constexpr int kResBlocks = 4;
+
+template <int BN, bool PAIR = false, bool RESB = false>
 struct Cfg {
   static constexpr int A_BYTES = kBlockM * kBlockK * 2;  // 16 KB
   // a CTA of a pair holds half of the tile's filter rows
   static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * kBlockK * 2;
-  static constexpr int STAGE = A_BYTES + B_BYTES;
-  static constexpr int STAGES = PAIR ? (BN == 256 ? 6 : 8) : (BN == 256 ? 4 : (BN == 128 ? 6 : 8));
-  static constexpr int PIPE = STAGE * STAGES;
+  static constexpr int STAGE = A_BYTES + (RESB ? 0 : B_BYTES);
+  static constexpr int STAGES =
+      RESB ? 8 : (PAIR ? (BN == 256 ? 6 : 8) : (BN == 256 ? 4 : (BN == 128 ? 6 : 8)));
+  static constexpr int RES_BYTES = RESB ? kResBlocks * B_BYTES : 0;  // after the stages
+  static constexpr int PIPE = STAGE * STAGES + RES_BYTES;
   static constexpr int EPI_STAGE = kEpiWarps * kStageWarpBytes;  // 32 KB
   static constexpr int BAR_BYTES = 256;
   static constexpr int NI = (BN == 256) ? 1 : 2;  // MMA issuer threads
@@ -87,8 +96,9 @@ struct Cfg {
   static constexpr int USED = PIPE + EPI_STAGE + kBiasBytes + BAR_BYTES;
   static constexpr int SMEM = kSmemLimit;
   static_assert(USED <= kSmemLimit, "exceeds the 227 KB of shared memory a CTA may use");
-  // full/empty per stage, tfull/tempty per TMEM buffer (up to 4), done per issuer
-  static_assert(2 * STAGES + 10 <= (BAR_BYTES - 8) / 8, "barrier area too small");
+  // full/empty per stage, tfull/tempty per TMEM buffer (up to 4), done per
+  // issuer, the resident filter's barrier
+  static_assert(2 * STAGES + 11 <= (BAR_BYTES - 8) / 8, "barrier area too small");
 };
 
 struct Work {
@@ -342,7 +352,7 @@ __device__ __forceinline__ void producer_advance(const ConvGemmParams& p, const 
 
 // VOL: the 3D (volume) paths are compiled in; the 2D kernels carry none of
 // their branches.
-template <int BN, bool PAIR, bool VOL>
+template <int BN, bool PAIR, bool VOL, bool RESB = false>
 __device__ __forceinline__ void issue_stage_loads(const ProdCtx& c, const ProducerPos& s,
                                                   uint8_t* sA, uint8_t* sB, uint64_t* bar) {
   const int kb = s.kb;
@@ -421,7 +431,9 @@ __device__ __forceinline__ void issue_stage_loads(const ProdCtx& c, const Produc
     // dense block-diagonal filter (fprop: filter columns; dgrad: filter rows)
     const int ch = group_window(c, s.w.tile_n) + cb * kBlockK;
     tma_load_im2col_4d(sA, s.mapA, bar, ch, s.base_w, s.base_h, s.img, off_w, off_h);
-    if (c.b_src == SRC_W_K) {
+    if (RESB) {
+      // the filter is resident in shared memory
+    } else if (c.b_src == SRC_W_K) {
       tma_load_4d(sB, c.mapB, bar, ch, sc, r, s.w.tile_n * BN);
     } else {
 #pragma unroll
@@ -508,11 +520,11 @@ __device__ __forceinline__ void issue_stage_loads(const ProdCtx& c, const Produc
   }
 }
 
-template <int BN, bool PAIR, bool VOL>
+template <int BN, bool PAIR, bool VOL, bool RESB = false>
 __device__ __forceinline__ void run_producer(const ConvGemmParams& p, uint8_t* pipe,
-                                             uint64_t* full, uint64_t* empty,
+                                             uint64_t* full, uint64_t* empty, uint64_t* bfull,
                                              volatile int* abort_flag, int pid, int lane) {
-  using C = Cfg<BN, PAIR>;
+  using C = Cfg<BN, PAIR, RESB>;
   constexpr int NP = C::NP;
   constexpr int OWN = C::STAGES / NP;  // stages this lane owns
   uint32_t last_phase[OWN];
@@ -545,6 +557,31 @@ __device__ __forceinline__ void run_producer(const ConvGemmParams& p, uint8_t* p
     pos.kb = pos.w.kb0 - NP;      // so that advancing by NP lands on kb0
     producer_advance<VOL>(p, c, pos, NP + pid);
   }
+  // Resident filter: every unit of the launch reduces over the same blocks
+  // of the single 64-wide column tile, so producer 0 loads them once, block
+  // kb at offset kb * B_BYTES after the stages, on their own barrier.
+  bool b_issued = false;
+  if (RESB && pid == 0 && pos.active) {
+    if (elect_one_sync()) {
+      const int nkb = pos.w.kb1 - pos.w.kb0;
+      uint8_t* res = pipe + C::STAGE * C::STAGES;
+      mbar_arrive_expect_tx(bfull, static_cast<uint32_t>(nkb * C::B_BYTES));
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int tap = kb / c.sc.cblocks;
+        const int cb = kb - tap * c.sc.cblocks;
+        const int jr = tap / pos.scount;
+        const int js = tap - jr * pos.scount;
+        const int r = pos.r0 + jr * pos.rstep;
+        const int sc = pos.s0 + js * pos.sstep;
+        if (c.b_src == SRC_W_K)
+          tma_load_4d(res + kb * C::B_BYTES, c.mapB, bfull, cb * kBlockK, sc, r, 0);
+        else
+          tma_load_4d(res + kb * C::B_BYTES, c.mapB, bfull, 0, sc, r, cb * kBlockK);
+      }
+    }
+    __syncwarp();
+    b_issued = true;
+  }
   int stage = pid;                // sequence number q = pid: stage q % STAGES
   uint32_t phase = 0;
   int slot = 0;                   // index of `stage` among this lane's stages
@@ -559,7 +596,7 @@ __device__ __forceinline__ void run_producer(const ConvGemmParams& p, uint8_t* p
       // with pairs the even CTA's barrier expects both CTAs' bytes
       if (!PAIR) mbar_arrive_expect_tx(&full[stage], C::STAGE);
       else if (c.sc.rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE);
-      issue_stage_loads<BN, PAIR, VOL>(c, pos, sA, sB, &full[stage]);
+      issue_stage_loads<BN, PAIR, VOL, RESB>(c, pos, sA, sB, &full[stage]);
     }
     __syncwarp();
     issued[slot] = true;
@@ -581,6 +618,8 @@ __device__ __forceinline__ void run_producer(const ConvGemmParams& p, uint8_t* p
     if (issued[s] && !mbar_wait(bar, last_phase[s], nullptr, timeout) && lane == 0)
       report_failure(p, abort_flag, DEVERR_TEARDOWN_WAIT);
   }
+  if (b_issued && !mbar_wait(bfull, 0u, nullptr, timeout) && lane == 0)
+    report_failure(p, abort_flag, DEVERR_TEARDOWN_WAIT);
 }
 
 // Position within its unit of issuer i's first block, the unit's first
@@ -624,12 +663,12 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 
 // With pairs only the even CTA runs this; its MMAs (M = 256) read both CTAs'
 // stages and write both CTAs' TMEM, and its commits arrive in both CTAs.
-template <int BN, bool PAIR>
+template <int BN, bool PAIR, bool RESB = false>
 __device__ __forceinline__ void run_mma(const ConvGemmParams& p, uint8_t* pipe, uint64_t* full,
                                         uint64_t* empty, uint64_t* tfull, uint64_t* tempty,
-                                        uint64_t* done_bar, uint32_t tmem_base,
+                                        uint64_t* done_bar, uint64_t* bfull, uint32_t tmem_base,
                                         volatile int* abort_flag, int issuer, int lane) {
-  using C = Cfg<BN, PAIR>;
+  using C = Cfg<BN, PAIR, RESB>;
   constexpr int NI = C::NI;
   constexpr int STAGES = C::STAGES;
   const Sched sc = load_sched<PAIR>(p);
@@ -657,9 +696,12 @@ __device__ __forceinline__ void run_mma(const ConvGemmParams& p, uint8_t* pipe, 
   const uint64_t a0 = taps    ? make_smem_desc_noswizzle(pipe_addr, 2048, 128)
                       : a_tmn ? make_smem_desc_noswizzle(pipe_addr, 128, 1024)
                               : make_smem_desc(pipe_addr, a_mn ? 8192 : 16, 1024);
+  // the resident filter (RESB) lies after the stages, one B_BYTES block per
+  // reduction block of the unit
+  const uint32_t b_base = RESB ? pipe_addr + C::STAGE * C::STAGES : pipe_addr + C::A_BYTES;
   const uint64_t b0 = taps    ? make_smem_desc_noswizzle(pipe_addr + C::A_BYTES, BN * 16, 128)
                       : b_tmn ? make_smem_desc_noswizzle(pipe_addr + C::A_BYTES, 128, 1024)
-                              : make_smem_desc(pipe_addr + C::A_BYTES, b_mn ? 8192 : 16, 1024);
+                              : make_smem_desc(b_base, b_mn ? 8192 : 16, 1024);
   const uint64_t ak = taps ? 4096 / 16 : (a_tmn ? 256 / 16 : (a_mn ? 2048 / 16 : 32 / 16));
   const uint64_t bk = taps ? 2 * BN * 16 / 16 : (b_tmn ? 256 / 16 : (b_mn ? 2048 / 16 : 32 / 16));
   constexpr uint32_t kStageUnits = C::STAGE / 16;
@@ -670,6 +712,13 @@ __device__ __forceinline__ void run_mma(const ConvGemmParams& p, uint8_t* pipe, 
   const int buf_shift = p.epi_groups == 2 ? 2 : 1;
   const int buf_mask = (1 << buf_shift) - 1;
   bool ok = true;
+  if (RESB && unit_first(sc) < sc.units) {  // producer 0 loads it when there is work
+    if (!__all_sync(0xffffffffu, mbar_wait(bfull, 0u, abort_flag, timeout))) {
+      if (lane == 0) report_failure(p, abort_flag, DEVERR_MMA_FULL_WAIT);
+      ok = false;
+    }
+    tc_fence_after_sync();
+  }
   UnitWalk uw;
   for (walk_begin(p, sc, uw); ok && uw.u < sc.units; walk_next(sc, uw)) {
     const Work w = walk_work(p, sc, uw);
@@ -700,7 +749,8 @@ __device__ __forceinline__ void run_mma(const ConvGemmParams& p, uint8_t* pipe, 
       }
       tc_fence_after_sync();
       const uint64_t ad = a0 + st * kStageUnits;
-      const uint64_t bd = b0 + st * kStageUnits;
+      const uint64_t bd =
+          RESB ? b0 + static_cast<uint64_t>(rel) * (C::B_BYTES / 16) : b0 + st * kStageUnits;
       if (elect_one_sync()) {
         mma_issue<PAIR>(d, ad, bd, idesc, acc);
         mma_issue<PAIR>(d, ad + ak, bd + bk, idesc, 1u);
@@ -1425,10 +1475,10 @@ __host__ __device__ constexpr uint32_t tmem_cols_for(uint32_t need) {
 
 // PAIR: launched as clusters of two CTAs (p.pair set), each pair working on
 // 256-row units with tcgen05.mma.cta_group::2 issued by the even CTA.
-template <int BN, bool PAIR, bool VOL>
+template <int BN, bool PAIR, bool VOL, bool RESB = false>
 __global__ void __launch_bounds__(kThreads, 1)
     conv_gemm_kernel(const __grid_constant__ ConvGemmParams p) {
-  using C = Cfg<BN, PAIR>;
+  using C = Cfg<BN, PAIR, RESB>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -1446,7 +1496,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tfull = empty + C::STAGES;
   uint64_t* tempty = tfull + 4;
   uint64_t* done_bar = tempty + 4;  // one per issuer
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 2);
+  uint64_t* bfull = done_bar + 2;   // the resident filter (RESB)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bfull + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -1469,6 +1520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&done_bar[0], 1);
     mbar_init(&done_bar[1], 1);
+    mbar_init(bfull, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -1523,13 +1575,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-    run_producer<BN, PAIR, VOL>(p, pipe, full, empty, abort_flag, warp, lane);
+    run_producer<BN, PAIR, VOL, RESB>(p, pipe, full, empty, bfull, abort_flag, warp, lane);
     }
   } else if (warp >= kMmaWarp0) {
     setmaxnreg_dec<kRegsLow>();
     if (warp < kMmaWarp0 + C::NI && (!PAIR || rank == 0))
-      run_mma<BN, PAIR>(p, pipe, full, empty, tfull, tempty, &done_bar[warp - kMmaWarp0],
-                        tmem_base, abort_flag, warp - kMmaWarp0, lane);
+      run_mma<BN, PAIR, RESB>(p, pipe, full, empty, tfull, tempty, &done_bar[warp - kMmaWarp0],
+                              bfull, tmem_base, abort_flag, warp - kMmaWarp0, lane);
   } else {
     setmaxnreg_inc<kRegsEpi>();
     run_epilogue<BN, PAIR, VOL>(p, tfull, tempty, tmem_base, abort_flag, warp, stage_buf, bias_s);
@@ -1566,6 +1618,7 @@ static cudaError_t launch_bn(const ConvGemmParams& p, int grid, cudaStream_t s) 
     // 3D problems take the kernel with the volume paths compiled in
     const bool vol = p.a_src == SRC_IM2COL_K3 || p.wg_Do > 0;
     auto* k = vol ? conv_gemm_kernel<BN, false, true> : conv_gemm_kernel<BN, false, false>;
+    if (BN == 64 && p.res_b && !vol) k = conv_gemm_kernel<64, false, false, true>;
     cudaError_t e = check_launch_regs(reinterpret_cast<const void*>(k));
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -1651,6 +1704,14 @@ cudaError_t launch_conv_gemm(const ConvGemmParams& p_in, int block_n, int grid, 
   ConvGemmParams p = p_in;
   const bool fits = block_n == 64 && !p.pair && p.epi != EPI_PARTIAL && 4 * p.num_acc * 64 <= 512;
   p.epi_groups = (fits && p.epi_groups != 1) ? 2 : 1;
+  // Resident filter (p.res_b set by the planner when allowed): 64-wide tiles
+  // of a single column tile and one sub-problem, whole-tile units, the
+  // filter a plain tiled operand, at most kResBlocks blocks per unit.
+  const bool res_ok = block_n == 64 && !p.pair && p.nsub == 1 && p.tiles_n == 1 &&
+                      p.grp_mul == 0 && p.epi != EPI_PARTIAL && p.a_src == SRC_IM2COL_K &&
+                      (p.b_src == SRC_W_K || p.b_src == SRC_W_MN) &&
+                      p.sub[0].rcount * p.sub[0].scount * p.cblocks <= kResBlocks;
+  p.res_b = p.res_b && res_ok ? 1 : 0;
   switch (block_n) {
     case 64: return p.pair ? launch_bn<64, true>(p, grid, s) : launch_bn<64, false>(p, grid, s);
     case 128: return p.pair ? launch_bn<128, true>(p, grid, s) : launch_bn<128, false>(p, grid, s);

@@ -87,6 +87,8 @@ struct ConvGemmParams {
   int store_box64;            // mapY boxes are 64 columns wide (128-byte swizzle)
   int nsub;
   int pair;                   // 1: clusters of two CTAs, 256-row units, cta_group::2 MMAs
+  int res_b;                  // 1: the filter may stay resident in shared memory (the launcher
+                              // keeps it only where a 64-wide single-column plan allows)
   int raster;                 // tile order of fprop / dgrad units: <= 1 column tiles fastest;
                               // g > 1 runs of g row tiles, rows fastest within a column
   int a_src, b_src;           // SrcKind

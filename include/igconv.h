@@ -590,6 +590,13 @@ IGCONV_API const char *igconv_status_string(igconv_status_t status);
  *                             fastest (the built-in order); g in 2..64 runs
  *                             of g row tiles, rows fastest within each
  *                             column.  Results are bit-identical.
+ *   IGCONV_TUNE_RESIDENT_FILTER  0: fprop / stride-1 dgrad plans with
+ *                             64-wide tiles, a single column tile and at
+ *                             most 4 reduction blocks per tile keep the
+ *                             whole filter in shared memory (loaded once
+ *                             per CTA; the pipeline stages then carry only
+ *                             the im2col rows); 1: never.  Results are
+ *                             bit-identical.
  * Returns INVALID_ARG for an unknown key or value. */
 typedef enum {
     IGCONV_TUNE_WGRAD_SPLITS = 1,
@@ -599,7 +606,8 @@ typedef enum {
     IGCONV_TUNE_EPI_GROUPS = 5,
     IGCONV_TUNE_CONV_SPLITS = 6,
     IGCONV_TUNE_FEW_CHANNELS = 7,
-    IGCONV_TUNE_RASTER = 8
+    IGCONV_TUNE_RASTER = 8,
+    IGCONV_TUNE_RESIDENT_FILTER = 9
 } igconv_tune_key_t;
 IGCONV_API igconv_status_t igconv_set_tuning(igconv_tune_key_t key, int value);
 

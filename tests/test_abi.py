@@ -172,6 +172,9 @@ def test_tuning_keys(igc):
     assert lib.igconv_set_tuning(igc.TUNE_RASTER, -1) == 1
     assert lib.igconv_set_tuning(igc.TUNE_RASTER, 8) == 0
     assert lib.igconv_set_tuning(igc.TUNE_RASTER, 0) == 0
+    assert lib.igconv_set_tuning(igc.TUNE_RESIDENT_FILTER, 2) == 1
+    assert lib.igconv_set_tuning(igc.TUNE_RESIDENT_FILTER, 1) == 0
+    assert lib.igconv_set_tuning(igc.TUNE_RESIDENT_FILTER, 0) == 0
 
 
 def test_grouped_reject_invalid(igc):

@@ -1,7 +1,9 @@
-"""The tile raster order of the persistent scheduler (IGCONV_TUNE_RASTER,
-the CUTLASS example's "Swizzling Stride"): every order computes every tile
-exactly once with the same reduction, so outputs are bit-identical to the
-built-in order (and exact against the oracle on integer data)."""
+"""Scheduling and staging knobs that must not change a bit: the tile raster
+order of the persistent scheduler (IGCONV_TUNE_RASTER, the CUTLASS
+example's "Swizzling Stride") and the shared-memory-resident filter
+(IGCONV_TUNE_RESIDENT_FILTER).  Every setting computes every tile exactly
+once with the same reduction, so outputs are bit-identical to the built-in
+setting (and exact against the oracle on integer data)."""
 import numpy as np
 import pytest
 import torch
@@ -51,3 +53,37 @@ def test_raster_orders_bit_identical(case):
         igc.igconv_set_tuning(igc.TUNE_RASTER, 0)
     for g, o in outs.items():
         assert np.array_equal(o, outs[0]), f"raster {g} differs from the built-in order"
+
+
+# Resident filter (IGCONV_TUNE_RESIDENT_FILTER): 64-wide single-column plans
+# with at most 4 reduction blocks keep the filter in shared memory; the
+# MMAs read the same operands, so results are bit-identical either way.
+RES_CASES = [
+    ("fprop", problem(2, 21, 23, 64, 64, 2, 2, (1, 1))),        # 4 blocks: resident
+    ("dgrad", problem(2, 19, 20, 64, 64, 2, 2, (1, 1))),        # stride-1 dgrad, 4 blocks
+    ("fprop", problem(2, 21, 23, 64, 64, 3, 3, (1, 1))),        # 9 blocks: not resident
+    ("dgrad", problem(2, 16, 17, 64, 256, 1, 1)),               # 1x1 dgrad: 4 blocks of K
+    ("fprop", problem(2, 40, 42, 3, 64, 7, 7, (3, 3), (2, 2))),  # packed stem: 4 blocks
+    ("fprop", problem(1, 15, 14, 128, 48, 3, 3, (1, 1))),       # 18 blocks: not resident
+]
+
+
+@pytest.mark.parametrize("case", RES_CASES, ids=lambda c: c[0] + "_" + "x".join(
+    str(c[1][k]) for k in "NHWCKRS"))
+def test_resident_filter_bit_identical(case):
+    kind, pb = case
+    inp, P, Q = inputs(pb, "f16", "int_uniform", 67, bias=True)
+    if kind == "fprop":
+        ref = oracle.fprop(pb, f64(inp["X"]), f64(inp["W"]), bias=f64(inp["bias"]), relu=True)
+    else:
+        ref = oracle.dgrad(pb, f64(inp["dY"]), f64(inp["W"]))
+    outs = []
+    try:
+        for off in (0, 1):
+            igc.igconv_set_tuning(igc.TUNE_RESIDENT_FILTER, off)
+            outs.append(run(kind, pb, inp))
+            device_ok()
+            assert_exact(outs[-1], ref, "f16", f"{kind} resident filter off={off}")
+    finally:
+        igc.igconv_set_tuning(igc.TUNE_RESIDENT_FILTER, 0)
+    assert np.array_equal(outs[0], outs[1])
