@@ -58,7 +58,7 @@ L2_FLUSH_BYTES = 512 << 20
 # kernel source hash (SHA-256 prefix of the kernel, its PTX wrappers and its
 # parameter header).  A changed kernel source reports null until it is
 # measured again.
-MEASURED_TRAFFIC = {"2990eb063bae77e8": 65.03e6}
+MEASURED_TRAFFIC = {"2990eb063bae77e8": 65.03e6, "676dfad8af80c5ea": 64.11e6}
 
 
 def conv_flops(pb, P, Q):
