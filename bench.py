@@ -729,15 +729,28 @@ def measure_rows(args, device, stream):
     # was measured on a 2 GB copy)
     copy_ms = time_call(lambda: dst.view(-1).copy_(src.view(-1)), stream, flush=flush)
     copy_gbs = nbytes / (copy_ms * 1e-3) / 1e9
-    for name, fn in (("nchw_to_nhwc", lambda: igc.nchw_to_nhwc(src, dst, N, C, H, W)),
-                     ("nhwc_to_nchw", lambda: igc.nhwc_to_nchw(dst, src, N, C, H, W))):
+    # streamed: 8 calls back to back over 4 buffer pairs (4 x 2 x 51 MB, more
+    # than the 129 MB L2, so every call reads its source from HBM), the time
+    # per call without one launch's ramp-up and tail
+    pairs = [(torch.randn((N, C, H, W), device=device).to(torch.bfloat16),
+              torch.empty((N, H, W, C), dtype=torch.bfloat16, device=device)) for _ in range(4)]
+    for name, fn, many in (
+            ("nchw_to_nhwc", lambda: igc.nchw_to_nhwc(src, dst, N, C, H, W),
+             lambda: [igc.nchw_to_nhwc(a, b, N, C, H, W) for _ in range(2) for a, b in pairs]),
+            ("nhwc_to_nchw", lambda: igc.nhwc_to_nchw(dst, src, N, C, H, W),
+             lambda: [igc.nhwc_to_nchw(b, a, N, C, H, W) for _ in range(2) for a, b in pairs])):
         ms = time_call(fn, stream, flush=flush)
         gbs = nbytes / (ms * 1e-3) / 1e9
+        ms8 = time_call(many, stream, reps=5, flush=flush) / 8
+        gbs8 = nbytes / (ms8 * 1e-3) / 1e9
         rows[name] = {"GB/s": gbs, "ms": ms, "shape": [N, C, H, W], "dtype": "bf16",
                       "bytes": nbytes, "frac_hbm": gbs / hbm, "hbm_gbs": hbm,
                       "hbm_source": peak_src, "copy_same_bytes_GB/s": copy_gbs,
-                      "frac_copy_same_bytes": gbs / copy_gbs}
-    del src, dst
+                      "frac_copy_same_bytes": gbs / copy_gbs,
+                      "streamed": {"GB/s": gbs8, "ms_per_call": ms8, "frac_hbm": gbs8 / hbm,
+                                   "how": "8 calls back to back over 4 buffer pairs "
+                                          "(411 MB, more than L2), time / 8"}}
+    del src, dst, pairs
     # dgrad/wgrad-heavy layers (dilated and strided), all three passes
     for name in ("dilated_112x112_64to64_3x3_d2", "strided_112x112_64to64_3x3_s2",
                  "cutlass_notebook"):
