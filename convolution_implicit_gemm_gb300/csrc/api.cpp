@@ -47,7 +47,7 @@ PFN_encodeTiled g_encode_tiled = nullptr;
 PFN_encodeIm2col g_encode_im2col = nullptr;
 std::atomic<int> g_tune_splits{0}, g_tune_bn{0}, g_tune_max_ctas{0}, g_tune_no_pairs{0},
     g_tune_epi_groups{0}, g_tune_conv_splits{0}, g_tune_few_channels{0}, g_tune_raster{0},
-    g_tune_resident_b{0};
+    g_tune_resident_b{0}, g_tune_dgrad_rows{0};
 
 igconv_status_t device_state(DeviceState** out) {
   int dev = 0;
@@ -228,6 +228,33 @@ void set_out_map_16(ConvGemmParams& p, void* base, long long rows, long long col
                         ? 1
                         : 0;
   p.store_box64 = wide ? p.use_tma_store : 0;
+}
+
+// Output map of a strided dgrad whose residue classes share one grid (see
+// padded_class_width): dX [N][H][W][C] viewed as (c, w % sw, w / sw, h % sh,
+// n * H / sh + h / sh), boxes of 32 grid columns of one class row, the box
+// width and staging swizzle chosen as in set_out_map_16.
+void set_out_map_dgrad_5d(ConvGemmParams& p, void* dX, const igconv_problem_t* pb, int bf16,
+                          int bn, int kblocks_per_tile) {
+  const bool wide = bn >= 128 && kblocks_per_tile <= 2;
+  const cuuint64_t px = static_cast<cuuint64_t>(pb->C) * 2;
+  const cuuint64_t dims[5] = {static_cast<cuuint64_t>(pb->C),
+                              static_cast<cuuint64_t>(pb->stride_w),
+                              static_cast<cuuint64_t>(pb->W / pb->stride_w),
+                              static_cast<cuuint64_t>(pb->stride_h),
+                              static_cast<cuuint64_t>(pb->N) * (pb->H / pb->stride_h)};
+  const cuuint64_t strides[4] = {px, px * pb->stride_w, px * pb->W,
+                                 px * pb->W * pb->stride_h};
+  const cuuint32_t box[5] = {wide ? 64u : 32u, 1, 32, 1, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  const CUresult r = g_encode_tiled(&p.mapY, tma_dtype(bf16), 5, dX, dims, strides, box, estr,
+                                    CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                    wide ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                                    CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  p.use_tma_store = r == CUDA_SUCCESS ? 1 : 0;
+  p.store_box64 = wide ? p.use_tma_store : 0;
+  if (!p.use_tma_store) p.store_5d = 0;  // padded rows stay valid through the row stores
 }
 
 // tcgen05 instruction descriptor, kind::f16 with an fp32 accumulator:
@@ -574,9 +601,21 @@ Residue1D residue_1d(int rho, int H, int R, int pad, int stride, int dil) {
   return d;
 }
 
+// Strided dgrad with H % stride_h == 0 and W % stride_w == 0: every residue
+// class has the same H / stride_h x W / stride_w grid.  Its rows are padded
+// to a multiple of 32 grid columns when that adds at most a sixth, so each
+// epilogue warp's 32 rows are one residue-class row of dX and go out as one
+// TMA store through a 5D view of dX (the padding columns are clipped).
+int padded_class_width(const igconv_problem_t* pb) {
+  if (pb->stride_h * pb->stride_w < 2 || pb->H % pb->stride_h || pb->W % pb->stride_w) return 0;
+  const int ws = pb->W / pb->stride_w;
+  const int wsp = ceil_div(ws, 32) * 32;
+  return 6 * (wsp - ws) <= ws ? wsp : 0;
+}
+
 igconv_status_t plan_dgrad(ConvGemmParams& p, int* block_n, const igconv_problem_t* pb, int P,
                            int Q, int bf16, const void* dY, const void* Wt, int sm_count,
-                           int forced_bn = 0) {
+                           int forced_bn = 0, bool pad_rows = false) {
   const int bn = forced_bn ? forced_bn
                            : choose_block_n(pb->C,
                                             ceil_div(static_cast<long long>(pb->N) * pb->H * pb->W,
@@ -585,6 +624,7 @@ igconv_status_t plan_dgrad(ConvGemmParams& p, int* block_n, const igconv_problem
   if (bn != 64 && bn != 128 && bn != 256) return IGCONV_ERR_INVALID_ARG;
   if (pb->stride_h * pb->stride_w > kMaxSub) return IGCONV_ERR_UNSUPPORTED;
   p.tiles_n = ceil_div(pb->C, bn);
+  const int wsp = pad_rows && g_tune_dgrad_rows.load() != 1 ? padded_class_width(pb) : 0;
   int nsub = 0, tile_begin = 0;
   for (int rh = 0; rh < pb->stride_h; ++rh) {
     const Residue1D dh = residue_1d(rh, pb->H, pb->R, pb->pad_h, pb->stride_h, pb->dil_h);
@@ -593,12 +633,14 @@ igconv_status_t plan_dgrad(ConvGemmParams& p, int* block_n, const igconv_problem
       const Residue1D dw = residue_1d(rw, pb->W, pb->S, pb->pad_w, pb->stride_w, pb->dil_w);
       if (dw.count == 0) continue;
       SubProblem& sp = p.sub[nsub];
-      const long long M = static_cast<long long>(pb->N) * dh.count * dw.count;
+      const int ws = wsp > 0 ? wsp : dw.count;  // grid columns per row
+      const long long M = static_cast<long long>(pb->N) * dh.count * ws;
       sp.M = static_cast<int>(M);
       sp.tile_begin = tile_begin;
       sp.tiles_m = ceil_div(M, kBlockM);
       sp.Hs = dh.count;
-      sp.Ws = dw.count;
+      sp.Ws = ws;
+      sp.ws_valid = wsp > 0 ? dw.count : 0;
       sp.lower_h = dh.delta_min;
       sp.lower_w = dw.delta_min;
       sp.trav_h = 1;
@@ -614,10 +656,15 @@ igconv_status_t plan_dgrad(ConvGemmParams& p, int* block_n, const igconv_problem
       sp.out_sw = pb->stride_w;
       if (taps) {
         // base rows of the traversal: [delta_min, delta_min + count - 1] over dY [P][Q]
+        // (padded rows: the traversal runs on past the grid, reading zeros;
+        // if the map cannot take that corner, plan without the padding)
         if (!encode_im2col(&p.mapA[nsub], dY, bf16, pb->N, P, Q, pb->K, dh.delta_min,
                            dw.delta_min, dh.count - P + dh.delta_min,
-                           dw.count - Q + dw.delta_min, 1, 1, kBlockM))
-          return IGCONV_ERR_UNSUPPORTED;
+                           ws - Q + dw.delta_min, 1, 1, kBlockM)) {
+          if (wsp == 0) return IGCONV_ERR_UNSUPPORTED;
+          p.mapA_valid = 0;
+          return plan_dgrad(p, block_n, pb, P, Q, bf16, dY, Wt, sm_count, forced_bn, false);
+        }
         p.mapA_valid |= 1u << nsub;
       }
       tile_begin += sp.tiles_m * p.tiles_n;
@@ -625,6 +672,7 @@ igconv_status_t plan_dgrad(ConvGemmParams& p, int* block_n, const igconv_problem
     }
   }
   p.nsub = nsub;
+  p.store_5d = wsp > 0 ? 1 : 0;  // the launcher encodes the 5D view of dX
   p.units = tile_begin;
   p.a_src = SRC_IM2COL_K;
   p.b_src = SRC_W_MN;
@@ -1349,6 +1397,10 @@ igconv_status_t igconv_set_tuning(igconv_tune_key_t key, int value) {
       if (value < 0 || value > 1) return IGCONV_ERR_INVALID_ARG;
       g_tune_resident_b.store(value);
       return IGCONV_OK;
+    case IGCONV_TUNE_DGRAD_ROWS:
+      if (value < 0 || value > 1) return IGCONV_ERR_INVALID_ARG;
+      g_tune_dgrad_rows.store(value);
+      return IGCONV_OK;
   }
   return IGCONV_ERR_INVALID_ARG;
 }
@@ -1506,6 +1558,12 @@ static igconv_status_t launch_dgrad_plan(ConvGemmParams& p, int bn, const igconv
     // one sub-problem whose tile rows are consecutive input pixels
     set_out_map_16(p, dX, static_cast<long long>(prob->N) * prob->H * prob->W, prob->C, bf16,
                    bn, p.sub[0].rcount * p.sub[0].scount * p.cblocks);
+  } else if (p.store_5d) {
+    // residue classes on one padded grid: 32-row boxes through the 5D view
+    int kb = 0;
+    for (int i = 0; i < p.nsub; ++i)
+      kb = std::max(kb, p.sub[i].rcount * p.sub[i].scount * p.cblocks);
+    set_out_map_dgrad_5d(p, dX, prob, bf16, bn, kb);
   }
   p.cin = beta != 0.0f ? Cin : nullptr;
   p.bias = nullptr;
@@ -1659,7 +1717,8 @@ igconv_status_t conv2d_dgrad_ws(const igconv_problem_t* prob, igconv_dtype_t dty
   init_common(p, dev);
   int bn = 0;
   const int bf16 = dtype == IGCONV_BF16 ? 1 : 0;
-  if ((st = plan_dgrad(p, &bn, prob, P, Q, bf16, dY, Wt, dev->sm_count)) != IGCONV_OK) return st;
+  if ((st = plan_dgrad(p, &bn, prob, P, Q, bf16, dY, Wt, dev->sm_count, 0, true)) != IGCONV_OK)
+    return st;
   if (workspace && !aligned16(workspace)) return IGCONV_ERR_MISALIGNED;
   const bool unit_stride = prob->stride_h == 1 && prob->stride_w == 1 && p.nsub == 1;
   int splits = 1;
@@ -2010,7 +2069,8 @@ igconv_status_t conv2d_grouped_dgrad_ws(const igconv_problem_t* prob, int groups
   int bn = 64;
   // the dense dgrad plan over the block-diagonal filter (read MN-major),
   // each dX channel tile reducing over its window of dY channels
-  if ((st = plan_dgrad(p, &bn, prob, P, Q, bf16, dY, workspace, dev->sm_count, 64)) != IGCONV_OK)
+  if ((st = plan_dgrad(p, &bn, prob, P, Q, bf16, dY, workspace, dev->sm_count, 64, true)) !=
+      IGCONV_OK)
     return st;
   p.cblocks = win.blocks;
   p.grp_mul = win.mul;

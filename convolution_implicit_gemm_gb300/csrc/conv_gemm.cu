@@ -189,33 +189,49 @@ __device__ __forceinline__ Work decode_unit(const ConvGemmParams& p, const Sched
   return w;
 }
 
-// Walks this CTA's work units (static stride gridDim.x).  With a single
-// sub-problem and no split (fprop, stride-1 dgrad) the tile coordinates
-// advance by a precomputed quotient and remainder, so a step costs no
-// division and no parameter loads.
+// Walks this CTA's work units (static stride gridDim.x).  Without a split
+// and in the built-in tile order (fprop, dgrad) the walk keeps the unit's
+// sub-problem and tile coordinates and advances them by a precomputed
+// quotient and remainder, so a step costs no division and no parameter
+// loads; only a step into the next sub-problem (the residue classes of a
+// strided dgrad) places the walk again from the unit index.
 struct UnitWalk {
   int u, stride;
-  int tm, tn;  // fast path: tile coordinates of unit u (tm in 128-row tiles)
-  int gq, gr;  // stride / tiles_n and stride % tiles_n
-  int mstep;   // 128-row tiles per unit row: 2 with pairs
-  int nk;      // fast path: reduction blocks per unit
+  int tm, tn;    // fast path: tile coordinates of unit u (tm in 128-row tiles)
+  int gq, gr;    // stride / tiles_n and stride % tiles_n
+  int mstep;     // 128-row tiles per unit row: 2 with pairs
+  int nk;        // fast path: reduction blocks per unit of the sub-problem
+  int sub;       // fast path: sub-problem of unit u
+  int sub_end;   // fast path: first unit past that sub-problem
   bool fast;
 };
+
+// Places a fast walk at unit it.u (< units).
+__device__ __forceinline__ void walk_seek(const ConvGemmParams& p, const Sched& sc,
+                                          UnitWalk& it) {
+  int i = 0;
+  while (i + 1 < sc.nsub && it.u >= p.sub[i + 1].tile_begin) ++i;
+  it.sub = i;
+  it.sub_end = i + 1 < sc.nsub ? p.sub[i + 1].tile_begin : sc.units;
+  const int local = it.u - p.sub[i].tile_begin;
+  const int um = local / sc.tiles_n;
+  it.tn = local - um * sc.tiles_n;
+  it.tm = it.mstep * um + sc.rank;
+  it.nk = p.sub[i].rcount * p.sub[i].scount * sc.cblocks;
+}
 
 __device__ __forceinline__ void walk_begin(const ConvGemmParams& p, const Sched& sc,
                                            UnitWalk& it) {
   it.u = unit_first(sc);
   it.stride = unit_stride(sc);
-  it.fast = sc.epi != EPI_PARTIAL && sc.nsub == 1 && sc.raster <= 1;
-  it.tm = it.tn = it.gq = it.gr = it.nk = 0;
+  it.fast = sc.epi != EPI_PARTIAL && sc.raster <= 1;
+  it.tm = it.tn = it.gq = it.gr = it.nk = it.sub = 0;
+  it.sub_end = sc.units;
   it.mstep = sc.pair ? 2 : 1;
   if (it.fast) {
-    const int um = it.u / sc.tiles_n;
-    it.tn = it.u - um * sc.tiles_n;
-    it.tm = it.mstep * um + sc.rank;
     it.gq = it.stride / sc.tiles_n;
     it.gr = it.stride - it.gq * sc.tiles_n;
-    it.nk = p.sub[0].rcount * p.sub[0].scount * sc.cblocks;
+    if (it.u < sc.units) walk_seek(p, sc, it);
   }
 }
 
@@ -223,7 +239,7 @@ __device__ __forceinline__ Work walk_work(const ConvGemmParams& p, const Sched& 
                                           const UnitWalk& it) {
   if (it.fast) {
     Work w;
-    w.sub = 0;
+    w.sub = it.sub;
     w.tile_m = it.tm;
     w.tile_n = it.tn;
     w.split = 0;
@@ -234,9 +250,14 @@ __device__ __forceinline__ Work walk_work(const ConvGemmParams& p, const Sched& 
   return decode_unit(p, sc, it.u);
 }
 
-__device__ __forceinline__ void walk_next(const Sched& sc, UnitWalk& it) {
+__device__ __forceinline__ void walk_next(const ConvGemmParams& p, const Sched& sc,
+                                          UnitWalk& it) {
   it.u += it.stride;
   if (it.fast) {
+    if (it.u >= it.sub_end) {
+      if (it.u < sc.units) walk_seek(p, sc, it);
+      return;
+    }
     it.tn += it.gr;
     it.tm += it.mstep * it.gq;
     if (it.tn >= sc.tiles_n) {
@@ -720,7 +741,7 @@ __device__ __forceinline__ void run_mma(const ConvGemmParams& p, uint8_t* pipe, 
     tc_fence_after_sync();
   }
   UnitWalk uw;
-  for (walk_begin(p, sc, uw); ok && uw.u < sc.units; walk_next(sc, uw)) {
+  for (walk_begin(p, sc, uw); ok && uw.u < sc.units; walk_next(p, sc, uw)) {
     const Work w = walk_work(p, sc, uw);
     const int nk = w.kb1 - w.kb0;
     if (nk <= 0) continue;  // no reduction: the epilogue writes beta*Cin alone
@@ -838,13 +859,30 @@ __device__ __forceinline__ void warp_store_rows(uint8_t* stage, const uint4* min
   __syncwarp();
 }
 
+// Where a warp's 32 output rows go in the output map: row y of a 2D
+// [rows][cols] map, or (strided dgrad, b >= 0) the line (b, tw.., a, hrow)
+// of the 5D view of dX, the 32 rows being grid columns tw .. tw + 31 of one
+// residue-class row (columns past the image are clipped by the map).
+struct OutAt {
+  int y;
+  int b, tw, a, hrow;
+};
+
+__device__ __forceinline__ void tma_store_out(const CUtensorMap* map, const void* src, int x,
+                                              const OutAt& at) {
+  if (at.b >= 0)
+    tma_store_5d(map, src, x, at.b, at.tw, at.a, at.hrow);
+  else
+    tma_store_2d(map, src, x, at.y);
+}
+
 // Stages one 32-row box (this lane's row: n16 16-byte pieces, n16 = 2 or 4)
 // in the warp's next staging buffer, in the 32-/64-byte TMA swizzle, then
-// stores it with one TMA store at tensor coordinates (x, y).  The buffer is
+// stores it with one TMA store at column x of the rows `at`.  The buffer is
 // reused only after the store that last read it has finished reading.
 __device__ __forceinline__ void warp_tma_store_box(uint8_t* stage, int& flip, const uint4* mine,
-                                                   int n16, const CUtensorMap* map, int x, int y,
-                                                   int lane) {
+                                                   int n16, const CUtensorMap* map, int x,
+                                                   const OutAt& at, int lane) {
   uint8_t* buf = stage + flip * kStageBufBytes;
   if (lane == 0) bulk_wait_group_read<1>();
   __syncwarp();
@@ -864,7 +902,7 @@ __device__ __forceinline__ void warp_tma_store_box(uint8_t* stage, int& flip, co
   fence_proxy_async_smem();
   __syncwarp();
   if (lane == 0) {
-    tma_store_2d(map, buf, x, y);
+    tma_store_out(map, buf, x, at);
     bulk_commit_group();
   }
   flip ^= 1;
@@ -983,6 +1021,7 @@ struct EpiCtx {
   int rq_exp;
   unsigned long long timeout;
   int use_tma;
+  int store5;           // TMA stores through the 5D strided-dgrad view (see OutAt)
   int box64;            // 16-bit output boxes of 64 columns (128-byte swizzle)
   int ws_rows_per_split;   // M_pad (wgrad)
   int int_acc;             // accumulators hold exact integers: sum and store them as int32
@@ -1018,6 +1057,7 @@ __device__ __forceinline__ void run_epilogue(const ConvGemmParams& p, uint64_t* 
   e.rq_exp = p.rq_exp;
   e.timeout = p.timeout_ns;
   e.use_tma = p.use_tma_store;
+  e.store5 = p.use_tma_store && p.store_5d && e.sc.epi == EPI_STORE;
   e.box64 = p.use_tma_store && p.store_box64 && e.sc.epi == EPI_STORE;
   e.ws_rows_per_split = p.tiles_m_total * kBlockM;
   e.int_acc = p.int_acc;
@@ -1056,7 +1096,7 @@ __device__ __forceinline__ void run_epilogue(const ConvGemmParams& p, uint64_t* 
   const int M0 = p.sub[0].M;  // GEMM rows when there is one sub-problem
   const bool one_sub = e.sc.nsub == 1;
   UnitWalk uw;
-  for (walk_begin(p, e.sc, uw); uw.u < e.sc.units; walk_next(e.sc, uw)) {
+  for (walk_begin(p, e.sc, uw); uw.u < e.sc.units; walk_next(p, e.sc, uw)) {
     const Work w = walk_work(p, e.sc, uw);
     const int nk = w.kb1 - w.kb0;
     const bool has_acc = nk > 0;
@@ -1098,7 +1138,9 @@ __device__ __forceinline__ void run_epilogue(const ConvGemmParams& p, uint64_t* 
                               __float_as_uint(acc[16 * h + 4 * i + 3]));
           if (e.use_tma)
             warp_tma_store_box(stage, flip, o, 4, e.mapY, w.tile_n * BN + j * 32 + h * 16,
-                               w.split * e.ws_rows_per_split + w.tile_m * kBlockM + quarter * 32,
+                               OutAt{w.split * e.ws_rows_per_split + w.tile_m * kBlockM +
+                                         quarter * 32,
+                                     -1, 0, 0, 0},
                                lane);
           else
             warp_store_rows(stage, o, 4, my_off, base + h * 64, lane);
@@ -1163,7 +1205,22 @@ __device__ __forceinline__ void run_epilogue(const ConvGemmParams& p, uint64_t* 
       }
     } else {
       const int m = w.tile_m * kBlockM + row;
-      const bool valid = m < (one_sub ? M0 : p.sub[w.sub].M);
+      bool valid = m < (one_sub ? M0 : p.sub[w.sub].M);
+      OutAt at{w.tile_m * kBlockM + quarter * 32, -1, 0, 0, 0};
+      if (e.store5) {
+        // the warp's 32 rows: one residue-class row of dX (grid width a
+        // multiple of 32), written through the 5D view
+        const SubProblem& sp = p.sub[w.sub];
+        const int per_plane = sp.Hs * sp.Ws;
+        const int m0 = at.y;
+        const int n = m0 / per_plane;
+        const int rem = m0 - n * per_plane;
+        const int th = rem / sp.Ws;
+        at.b = sp.out_w0;
+        at.tw = rem - th * sp.Ws;
+        at.a = sp.out_h0;
+        at.hrow = n * sp.Hs + th;
+      }
       long long row_off = 0;  // elements; only the row-store and Cin paths use it
       if (valid && (!e.use_tma || e.beta != 0.0f)) {
         const SubProblem& sp = p.sub[w.sub];
@@ -1185,6 +1242,7 @@ __device__ __forceinline__ void run_epilogue(const ConvGemmParams& p, uint64_t* 
         }
         const int th = rem / Ws;
         const int tw = rem - th * Ws;
+        if (sp.ws_valid > 0 && tw >= sp.ws_valid) valid = false;  // row padding
         const int oh = sp.out_h0 + sp.out_sh * th;
         const int ow = sp.out_w0 + sp.out_sw * tw;
         row_off = ((img_row * e.out_H + oh) * e.out_W + ow) * static_cast<long long>(e.out_C);
@@ -1308,8 +1366,7 @@ __device__ __forceinline__ void run_epilogue(const ConvGemmParams& p, uint64_t* 
           const uint4 o[2] = {make_uint4(packed[0], packed[1], packed[2], packed[3]),
                               make_uint4(packed[4], packed[5], packed[6], packed[7])};
           if (e.use_tma)
-            warp_tma_store_box(stage, flip, o, 2, e.mapY, n0, w.tile_m * kBlockM + quarter * 32,
-                               lane);
+            warp_tma_store_box(stage, flip, o, 2, e.mapY, n0, at, lane);
           else
             warp_store_rows(stage, o, ncols / 16, valid ? row_off : -1LL,
                             static_cast<uint8_t*>(e.out) + n0, lane);
@@ -1349,7 +1406,7 @@ __device__ __forceinline__ void run_epilogue(const ConvGemmParams& p, uint64_t* 
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_store_2d(e.mapY, stage, n0, w.tile_m * kBlockM + quarter * 32);
+              tma_store_out(e.mapY, stage, n0, at);
               bulk_commit_group();
             }
             ++j;          // the pair's second chunk is done
@@ -1432,13 +1489,12 @@ __device__ __forceinline__ void run_epilogue(const ConvGemmParams& p, uint64_t* 
               fence_proxy_async_smem();
               __syncwarp();
               if (lane == 0) {
-                tma_store_2d(e.mapY, stage, n0 - 32 * hh, w.tile_m * kBlockM + quarter * 32);
+                tma_store_out(e.mapY, stage, n0 - 32 * hh, at);
                 bulk_commit_group();
               }
             }
           } else if (e.use_tma)
-            warp_tma_store_box(stage, flip, o, 4, e.mapY, n0, w.tile_m * kBlockM + quarter * 32,
-                               lane);
+            warp_tma_store_box(stage, flip, o, 4, e.mapY, n0, at, lane);
           else
             warp_store_rows(stage, o, ncols / 8, valid ? row_off * 2 : -1LL,
                             static_cast<uint8_t*>(e.out) + static_cast<long long>(n0) * 2, lane);

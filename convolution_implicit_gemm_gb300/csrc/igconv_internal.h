@@ -69,6 +69,8 @@ struct SubProblem {
   int r0, rstep, rcount, offh0, doffh;  // tap j: filter row r0 + j*rstep, im2col offset offh0 + j*doffh
   int s0, sstep, scount, offw0, doffw;
   int out_h0, out_w0, out_sh, out_sw;   // epilogue: output row = out_h0 + out_sh * grid row
+  int ws_valid;           // 0: every grid column is an output; else grid columns >= ws_valid
+                          // pad the row to Ws (their results are dropped)
   // 3D (Ds > 0): traversal depth, its lower corner and stride.  The r taps
   // run over the merged index jt * rdiv + jr (rcount = depth taps * rdiv):
   // filter row coordinate r0 + jt * tstride + jr * rstep of the [K][T*R]
@@ -84,6 +86,9 @@ struct ConvGemmParams {
   SubProblem sub[kMaxSub];
   uint32_t mapA_valid;        // bit i: mapA[i] holds an encoded map
   int use_tma_store;          // output tile rows are contiguous: store them with TMA
+  int store_5d;               // strided dgrad: mapY is dX viewed as (c, w % sw, w / sw, h % sh,
+                              // n * H / sh + h / sh), a residue class's grid row is one
+                              // (h % sh, row) line and each 32-row box lies inside one
   int store_box64;            // mapY boxes are 64 columns wide (128-byte swizzle)
   int nsub;
   int pair;                   // 1: clusters of two CTAs, 256-row units, cta_group::2 MMAs

@@ -597,6 +597,14 @@ IGCONV_API const char *igconv_status_string(igconv_status_t status);
  *                             per CTA; the pipeline stages then carry only
  *                             the im2col rows); 1: never.  Results are
  *                             bit-identical.
+ *   IGCONV_TUNE_DGRAD_ROWS    strided dgrad (stride_h * stride_w > 1) with
+ *                             H and W divisible by the strides: 0 pads each
+ *                             residue class's rows to a multiple of 32
+ *                             grid columns where that adds at most a sixth,
+ *                             and writes dX through TMA stores of whole
+ *                             class rows (the built-in choice); 1 never:
+ *                             every output pixel is stored by its own row
+ *                             address.  Results are bit-identical.
  * Returns INVALID_ARG for an unknown key or value. */
 typedef enum {
     IGCONV_TUNE_WGRAD_SPLITS = 1,
@@ -607,7 +615,8 @@ typedef enum {
     IGCONV_TUNE_CONV_SPLITS = 6,
     IGCONV_TUNE_FEW_CHANNELS = 7,
     IGCONV_TUNE_RASTER = 8,
-    IGCONV_TUNE_RESIDENT_FILTER = 9
+    IGCONV_TUNE_RESIDENT_FILTER = 9,
+    IGCONV_TUNE_DGRAD_ROWS = 10
 } igconv_tune_key_t;
 IGCONV_API igconv_status_t igconv_set_tuning(igconv_tune_key_t key, int value);
 

@@ -175,6 +175,9 @@ def test_tuning_keys(igc):
     assert lib.igconv_set_tuning(igc.TUNE_RESIDENT_FILTER, 2) == 1
     assert lib.igconv_set_tuning(igc.TUNE_RESIDENT_FILTER, 1) == 0
     assert lib.igconv_set_tuning(igc.TUNE_RESIDENT_FILTER, 0) == 0
+    assert lib.igconv_set_tuning(igc.TUNE_DGRAD_ROWS, 2) == 1
+    assert lib.igconv_set_tuning(igc.TUNE_DGRAD_ROWS, 1) == 0
+    assert lib.igconv_set_tuning(igc.TUNE_DGRAD_ROWS, 0) == 0
 
 
 def test_grouped_reject_invalid(igc):
