@@ -86,7 +86,8 @@ def kernel_source_hash():
     """sha256 prefix over the implicit-GEMM kernel's sources (the kernel, its
     PTX wrappers and the shared parameter header)."""
     h = hashlib.sha256()
-    for name in ("conv_gemm.cu", "ptx.cuh", "igconv_internal.h"):
+    for name in ("conv_gemm_kernel.cuh", "conv_gemm.cu", "conv_gemm_s16.cu", "ptx.cuh",
+                 "igconv_internal.h"):
         with open(os.path.join(ROOT, "convolution_implicit_gemm_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

@@ -47,7 +47,7 @@ PFN_encodeTiled g_encode_tiled = nullptr;
 PFN_encodeIm2col g_encode_im2col = nullptr;
 std::atomic<int> g_tune_splits{0}, g_tune_bn{0}, g_tune_max_ctas{0}, g_tune_no_pairs{0},
     g_tune_epi_groups{0}, g_tune_conv_splits{0}, g_tune_few_channels{0}, g_tune_raster{0},
-    g_tune_resident_b{0}, g_tune_dgrad_rows{0};
+    g_tune_resident_b{0}, g_tune_dgrad_rows{0}, g_tune_general_epi{0};
 
 igconv_status_t device_state(DeviceState** out) {
   int dev = 0;
@@ -351,6 +351,7 @@ void init_common(ConvGemmParams& p, const DeviceState* st) {
   p.epi_groups = g_tune_epi_groups.load();  // 0: the launcher decides
   p.raster = g_tune_raster.load();          // 0: column tiles fastest
   p.res_b = g_tune_resident_b.load() == 1 ? 0 : 1;  // the launcher decides where it applies
+  p.general_epilogue = g_tune_general_epi.load();
 }
 
 // fprop plan (16-bit, or the int8 path's widened copies) on X [N,H,W,C],
@@ -1400,6 +1401,10 @@ igconv_status_t igconv_set_tuning(igconv_tune_key_t key, int value) {
     case IGCONV_TUNE_DGRAD_ROWS:
       if (value < 0 || value > 1) return IGCONV_ERR_INVALID_ARG;
       g_tune_dgrad_rows.store(value);
+      return IGCONV_OK;
+    case IGCONV_TUNE_EPILOGUE_KERNEL:
+      if (value < 0 || value > 1) return IGCONV_ERR_INVALID_ARG;
+      g_tune_general_epi.store(value);
       return IGCONV_OK;
   }
   return IGCONV_ERR_INVALID_ARG;

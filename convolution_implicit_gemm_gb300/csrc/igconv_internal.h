@@ -86,6 +86,7 @@ struct ConvGemmParams {
   SubProblem sub[kMaxSub];
   uint32_t mapA_valid;        // bit i: mapA[i] holds an encoded map
   int use_tma_store;          // output tile rows are contiguous: store them with TMA
+  int general_epilogue;       // 1: 16-bit store plans run on the kernels with every epilogue
   int store_5d;               // strided dgrad: mapY is dX viewed as (c, w % sw, w / sw, h % sh,
                               // n * H / sh + h / sh), a residue class's grid row is one
                               // (h % sh, row) line and each 32-row box lies inside one
@@ -153,6 +154,9 @@ struct ConvGemmParams {
 
 // Launches the persistent implicit-GEMM kernel with tile width block_n.
 cudaError_t launch_conv_gemm(const ConvGemmParams& p, int block_n, int grid, cudaStream_t s);
+// The same launch on the kernels whose epilogue holds only the 16-bit store
+// path (a plan with EPI_STORE, 16-bit outputs and no 3D operands).
+cudaError_t launch_conv_gemm_s16(const ConvGemmParams& p, int block_n, int grid, cudaStream_t s);
 // Clusters of two CTAs of the kernel with this tile width that fit at once.
 int conv_gemm_pair_capacity(int block_n);
 size_t conv_gemm_smem_bytes(int block_n);

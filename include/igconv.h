@@ -605,6 +605,11 @@ IGCONV_API const char *igconv_status_string(igconv_status_t status);
  *                             class rows (the built-in choice); 1 never:
  *                             every output pixel is stored by its own row
  *                             address.  Results are bit-identical.
+ *   IGCONV_TUNE_EPILOGUE_KERNEL  0: 2D fprop / dgrad plans with 16-bit
+ *                             outputs run on kernels whose epilogue holds
+ *                             only that store path (the built-in choice);
+ *                             1: on the kernels that carry every epilogue.
+ *                             Results are bit-identical.
  * Returns INVALID_ARG for an unknown key or value. */
 typedef enum {
     IGCONV_TUNE_WGRAD_SPLITS = 1,
@@ -616,7 +621,8 @@ typedef enum {
     IGCONV_TUNE_FEW_CHANNELS = 7,
     IGCONV_TUNE_RASTER = 8,
     IGCONV_TUNE_RESIDENT_FILTER = 9,
-    IGCONV_TUNE_DGRAD_ROWS = 10
+    IGCONV_TUNE_DGRAD_ROWS = 10,
+    IGCONV_TUNE_EPILOGUE_KERNEL = 11
 } igconv_tune_key_t;
 IGCONV_API igconv_status_t igconv_set_tuning(igconv_tune_key_t key, int value);
 
