@@ -7,6 +7,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <climits>
 #include <cstring>
 #include <mutex>
 
@@ -47,7 +48,7 @@ PFN_encodeTiled g_encode_tiled = nullptr;
 PFN_encodeIm2col g_encode_im2col = nullptr;
 std::atomic<int> g_tune_splits{0}, g_tune_bn{0}, g_tune_max_ctas{0}, g_tune_no_pairs{0},
     g_tune_epi_groups{0}, g_tune_conv_splits{0}, g_tune_few_channels{0}, g_tune_raster{0},
-    g_tune_resident_b{0}, g_tune_dgrad_rows{0}, g_tune_general_epi{0};
+    g_tune_resident_b{0}, g_tune_dgrad_rows{0}, g_tune_general_epi{0}, g_tune_halo{0};
 
 igconv_status_t device_state(DeviceState** out) {
   int dev = 0;
@@ -230,31 +231,91 @@ void set_out_map_16(ConvGemmParams& p, void* base, long long rows, long long col
   p.store_box64 = wide ? p.use_tma_store : 0;
 }
 
-// Output map of a strided dgrad whose residue classes share one grid (see
-// padded_class_width): dX [N][H][W][C] viewed as (c, w % sw, w / sw, h % sh,
-// n * H / sh + h / sh), boxes of 32 grid columns of one class row, the box
-// width and staging swizzle chosen as in set_out_map_16.
-void set_out_map_dgrad_5d(ConvGemmParams& p, void* dX, const igconv_problem_t* pb, int bf16,
-                          int bn, int kblocks_per_tile) {
+// Output map for plans whose grid rows are whole output-row lines: the
+// output [N][H][W][C] viewed as (c, w % sw, w / sw, h % sh, n * H/sh + h/sh)
+// (H and W multiples of sh and sw), boxes of 32 grid columns of one line,
+// the box width and staging swizzle chosen as in set_out_map_16.  Used by the
+// strided dgrad's residue classes on one padded grid (padded_class_width)
+// and by halo plans (sh = sw = 1).
+void set_out_map_lines_5d(ConvGemmParams& p, void* out, int N, int H, int W, int C, int sh,
+                          int sw, int bf16, int bn, int kblocks_per_tile) {
   const bool wide = bn >= 128 && kblocks_per_tile <= 2;
-  const cuuint64_t px = static_cast<cuuint64_t>(pb->C) * 2;
-  const cuuint64_t dims[5] = {static_cast<cuuint64_t>(pb->C),
-                              static_cast<cuuint64_t>(pb->stride_w),
-                              static_cast<cuuint64_t>(pb->W / pb->stride_w),
-                              static_cast<cuuint64_t>(pb->stride_h),
-                              static_cast<cuuint64_t>(pb->N) * (pb->H / pb->stride_h)};
-  const cuuint64_t strides[4] = {px, px * pb->stride_w, px * pb->W,
-                                 px * pb->W * pb->stride_h};
+  const cuuint64_t px = static_cast<cuuint64_t>(C) * 2;
+  const cuuint64_t dims[5] = {static_cast<cuuint64_t>(C), static_cast<cuuint64_t>(sw),
+                              static_cast<cuuint64_t>(W / sw), static_cast<cuuint64_t>(sh),
+                              static_cast<cuuint64_t>(N) * (H / sh)};
+  const cuuint64_t strides[4] = {px, px * sw, px * W, px * W * sh};
   const cuuint32_t box[5] = {wide ? 64u : 32u, 1, 32, 1, 1};
   const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-  const CUresult r = g_encode_tiled(&p.mapY, tma_dtype(bf16), 5, dX, dims, strides, box, estr,
+  const CUresult r = g_encode_tiled(&p.mapY, tma_dtype(bf16), 5, out, dims, strides, box, estr,
                                     CU_TENSOR_MAP_INTERLEAVE_NONE,
                                     wide ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                                     CU_TENSOR_MAP_L2_PROMOTION_NONE,
                                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   p.use_tma_store = r == CUDA_SUCCESS ? 1 : 0;
   p.store_box64 = wide ? p.use_tma_store : 0;
-  if (!p.use_tma_store) p.store_5d = 0;  // padded rows stay valid through the row stores
+  p.store_5d = p.use_tma_store;  // otherwise the padded rows stay valid through the row stores
+}
+
+// Halo plan (conv_gemm_kernel.cuh, "Halo tiles") for the stride-1 plan in p
+// (fprop over X, or stride-1 dgrad over dY: one sub-problem, 64-wide tiles,
+// one column tile, one 64-channel reduction block, 2..kHaloTaps taps with
+// non-negative offsets) over the input in [N][Hin][Win][Cin] with an output
+// of Hout x Wout pixels.  The grid width Wt is the smallest of 32, 64, 128
+// that holds a padded input row (Wout + the largest column offset), so a
+// 128-row tile is 128 / Wt whole output rows, and needs Hout to be a multiple
+// of that; the halo of HR = 128 / Wt + the largest row offset + 1 rows of Wt
+// pixels must fit kHaloRows.  Rewrites p (input map, grid, units) and
+// returns true when the plan qualifies and IGCONV_TUNE_HALO allows it.
+bool try_halo_plan(ConvGemmParams& p, int bn, const void* in, int N, int Hin, int Win, int Cin,
+                   int Hout, int Wout, int bf16) {
+  if (g_tune_halo.load() == 1) return false;  // 0 built-in, 1 never
+  const SubProblem& sp = p.sub[0];
+  if (bn != 64 || p.pair || p.conv_split || p.nsub != 1 || p.tiles_n != 1 || p.cblocks != 1 ||
+      p.grp_mul != 0 || p.a_src != SRC_IM2COL_K ||
+      (p.b_src != SRC_W_K && p.b_src != SRC_W_MN) || sp.trav_h != 1 || sp.trav_w != 1 ||
+      sp.Ds > 0 || sp.tile_begin != 0)
+    return false;
+  const int taps = sp.rcount * sp.scount;
+  if (taps < 2 || taps > kHaloTaps) return false;
+  const int oh1 = sp.offh0 + (sp.rcount - 1) * sp.doffh;
+  const int ow1 = sp.offw0 + (sp.scount - 1) * sp.doffw;
+  if (std::min(sp.offh0, oh1) < 0 || std::min(sp.offw0, ow1) < 0) return false;
+  const int max_h = std::max(sp.offh0, oh1), max_w = std::max(sp.offw0, ow1);
+  int wt = 32;
+  while (wt < Wout + max_w && wt < 256) wt *= 2;
+  if (wt > 128 || wt < Wout + max_w) return false;
+  const int rows = kBlockM / wt;
+  const int hr = rows + max_h + 1;
+  if (hr * wt > kHaloRows || hr > 256 || Hout % rows != 0) return false;
+  const long long M = static_cast<long long>(N) * Hout * wt;
+  if (M > INT_MAX) return false;
+  // the input, box (64 channels, wt pixels, hr rows, one image); padding
+  // and the columns past the image read as zero
+  CUtensorMap map;
+  const cuuint64_t px = static_cast<cuuint64_t>(Cin) * 2;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(Cin), static_cast<cuuint64_t>(Win),
+                              static_cast<cuuint64_t>(Hin), static_cast<cuuint64_t>(N)};
+  const cuuint64_t strides[3] = {px, px * Win, px * Win * Hin};
+  const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(wt), static_cast<cuuint32_t>(hr), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  if (g_encode_tiled(&map, tma_dtype(bf16), 4, const_cast<void*>(in), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  p.mapA[0] = map;
+  p.mapA_valid = 1u;
+  SubProblem& s = p.sub[0];
+  s.M = static_cast<int>(M);
+  s.tiles_m = static_cast<int>(M / kBlockM);
+  s.Ws = wt;
+  s.ws_valid = Wout;
+  p.units = s.tiles_m;
+  p.halo = 1;
+  p.halo_bytes = hr * wt * 128;
+  p.res_b = 0;
+  return true;
 }
 
 // tcgen05 instruction descriptor, kind::f16 with an fp32 accumulator:
@@ -1406,6 +1467,10 @@ igconv_status_t igconv_set_tuning(igconv_tune_key_t key, int value) {
       if (value < 0 || value > 1) return IGCONV_ERR_INVALID_ARG;
       g_tune_general_epi.store(value);
       return IGCONV_OK;
+    case IGCONV_TUNE_HALO:
+      if (value < 0 || value > 1) return IGCONV_ERR_INVALID_ARG;
+      g_tune_halo.store(value);
+      return IGCONV_OK;
   }
   return IGCONV_ERR_INVALID_ARG;
 }
@@ -1527,9 +1592,16 @@ igconv_status_t conv2d_fprop_ws(const igconv_problem_t* prob, igconv_dtype_t dty
   }
   p.epi = EPI_STORE;
   p.out = Y;
-  // output tile rows are consecutive pixels: store them with TMA
-  set_out_map_16(p, Y, static_cast<long long>(prob->N) * P * Q, prob->K, bf16, bn,
-                 p.sub[0].rcount * p.sub[0].scount * p.cblocks);
+  if (!few && splits == 1 && !p.pair && prob->stride_h == 1 && prob->stride_w == 1 &&
+      try_halo_plan(p, bn, X, prob->N, prob->H, prob->W, prob->C, P, Q, bf16)) {
+    // halo plan: grid rows are whole output rows
+    set_out_map_lines_5d(p, Y, prob->N, P, Q, prob->K, 1, 1, bf16, bn,
+                         p.sub[0].rcount * p.sub[0].scount * p.cblocks);
+  } else {
+    // output tile rows are consecutive pixels: store them with TMA
+    set_out_map_16(p, Y, static_cast<long long>(prob->N) * P * Q, prob->K, bf16, bn,
+                   p.sub[0].rcount * p.sub[0].scount * p.cblocks);
+  }
   if (!few) {  // the few-channel filter copy was just written: it is in L2
     p.pf_base = Wt;
     p.pf_bytes = static_cast<long long>(prob->K) * prob->R * prob->S * prob->C * 2;
@@ -1559,7 +1631,11 @@ static igconv_status_t launch_dgrad_plan(ConvGemmParams& p, int bn, const igconv
                                          int bf16, const DeviceState* dev, cudaStream_t stream) {
   p.epi = EPI_STORE;
   p.out = dX;
-  if (prob->stride_h == 1 && prob->stride_w == 1) {
+  if (p.halo) {
+    // halo plan: grid rows are whole dX rows
+    set_out_map_lines_5d(p, dX, prob->N, prob->H, prob->W, prob->C, 1, 1, bf16, bn,
+                         p.sub[0].rcount * p.sub[0].scount * p.cblocks);
+  } else if (prob->stride_h == 1 && prob->stride_w == 1) {
     // one sub-problem whose tile rows are consecutive input pixels
     set_out_map_16(p, dX, static_cast<long long>(prob->N) * prob->H * prob->W, prob->C, bf16,
                    bn, p.sub[0].rcount * p.sub[0].scount * p.cblocks);
@@ -1568,7 +1644,8 @@ static igconv_status_t launch_dgrad_plan(ConvGemmParams& p, int bn, const igconv
     int kb = 0;
     for (int i = 0; i < p.nsub; ++i)
       kb = std::max(kb, p.sub[i].rcount * p.sub[i].scount * p.cblocks);
-    set_out_map_dgrad_5d(p, dX, prob, bf16, bn, kb);
+    set_out_map_lines_5d(p, dX, prob->N, prob->H, prob->W, prob->C, prob->stride_h,
+                         prob->stride_w, bf16, bn, kb);
   }
   p.cin = beta != 0.0f ? Cin : nullptr;
   p.bias = nullptr;
@@ -1750,6 +1827,8 @@ igconv_status_t conv2d_dgrad_ws(const igconv_problem_t* prob, igconv_dtype_t dty
     p.pair = 1;
     p.units = ceil_div(p.sub[0].tiles_m, 2) * p.tiles_n;
     p.idesc = make_idesc(2 * kBlockM, bn, bf16, 0, 1);
+  } else if (unit_stride) {
+    try_halo_plan(p, bn, dY, prob->N, P, Q, prob->K, prob->H, prob->W, bf16);
   }
   p.pf_base = Wt;
   p.pf_bytes = static_cast<long long>(prob->K) * prob->R * prob->S * prob->C * 2;

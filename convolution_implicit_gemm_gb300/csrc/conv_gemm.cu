@@ -75,6 +75,11 @@ cudaError_t launch_conv_gemm(const ConvGemmParams& p_in, int block_n, int grid, 
   // plain 16-bit stores (fprop, dgrad) take the kernels whose epilogue
   // holds only that path, unless the plan asks for the general ones
   const bool vol = p.a_src == SRC_IM2COL_K3 || p.wg_Do > 0;
+  if (p.halo) {
+    if (block_n != 64 || p.pair || p.epi != EPI_STORE || p.out_f32 || p.int_acc || vol)
+      return cudaErrorInvalidValue;
+    return launch_conv_gemm_halo(p, grid, s);
+  }
   if (p.epi == EPI_STORE && !p.out_f32 && !p.int_acc && !vol && !p.general_epilogue)
     return launch_conv_gemm_s16(p, block_n, grid, s);
   return launch_block_n<false>(p, block_n, grid, s);

@@ -1664,6 +1664,301 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Halo tiles (stride-1 fprop and dgrad, one 64-channel reduction block, one
+// 64-wide column tile, at most kHaloTaps filter taps).  Output positions are
+// indexed on a grid whose rows are Wt columns wide (Wt = 32, 64 or 128, at
+// least the padded input row), so a 128-row tile is 128 / Wt whole output
+// rows of one image.  Every filter tap of such a tile reads the same input
+// rows shifted by (off_h * Wt + off_w) grid positions, so one TMA copy of
+// the tile's input rows -- the halo: HR = 128 / Wt + (R-1) dil_h + 1 rows of
+// Wt pixels, zero outside the image -- feeds all its reduction blocks,
+// instead of one im2col copy per tap.  The filter stays resident in shared
+// memory.  A block's A operand is the 128 halo rows starting at its offset:
+// the descriptor's start moves by whole 128-byte pixel rows, also to rows
+// that are not on an 8-row (1024-byte) swizzle boundary.  The 128-byte
+// swizzle is a function of the absolute shared-memory address (the 16-byte
+// chunk index XOR address bits 7-9), for the TMA that writes the halo and
+// the MMA that reads it alike, so the base-offset field stays zero (checked
+// on the GPU: with the field set to the start's row within the pattern the
+// products were wrong, with it zero exact).  Both issuers read every halo
+// (each takes the blocks of its sequence parity), so a halo stage is free
+// once both have committed.  Junk columns (grid column >= the output width)
+// read neighbouring pixels; the epilogue drops them (ws_valid, and the
+// output map clips them).
+// ---------------------------------------------------------------------------
+struct HaloCfg {
+  static constexpr int STAGE = 40960;                    // up to 320 rows of 128 bytes
+  static constexpr int STAGES = 3;
+  static constexpr int B_BYTES = 64 * kBlockK * 2;       // one 64 x 64 filter block
+  static constexpr int RES_BYTES = kHaloTaps * B_BYTES;  // after the stages
+  static constexpr int PIPE = STAGE * STAGES + RES_BYTES;
+  static constexpr int EPI_STAGE = kEpiWarps * kStageWarpBytes;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int NI = 2;
+  static constexpr int NP = STAGES;  // producer warp i owns stage i
+  static constexpr int USED = PIPE + EPI_STAGE + kBiasBytes + BAR_BYTES;
+  static constexpr int SMEM = kSmemLimit;
+  static_assert(USED <= kSmemLimit, "exceeds the 227 KB of shared memory a CTA may use");
+  static_assert(STAGE % 1024 == 0 && PIPE % 1024 == 0, "swizzle atoms need 1024-byte alignment");
+  static_assert(2 * STAGES + 11 <= (BAR_BYTES - 8) / 8, "barrier area too small");
+};
+
+// Producer warp `pid` (0..2) fills halo stage pid for every third unit of
+// this CTA; producer 0 first loads the resident filter.
+__device__ __forceinline__ void run_producer_halo(const ConvGemmParams& p, uint8_t* pipe,
+                                                  uint64_t* full, uint64_t* empty,
+                                                  uint64_t* bfull, volatile int* abort_flag,
+                                                  int pid, int lane) {
+  using C = HaloCfg;
+  const Sched sc = load_sched<false>(p);
+  const unsigned long long timeout = p.timeout_ns;
+  const int Wt = p.sub[0].Ws;
+  const int per_img = p.sub[0].Hs * Wt;
+  const int lower_h = p.sub[0].lower_h, lower_w = p.sub[0].lower_w;
+  const uint32_t bytes = static_cast<uint32_t>(p.halo_bytes);
+  const CUtensorMap* map = &p.mapA[0];
+  bool b_issued = false;
+  if (pid == 0 && unit_first(sc) < sc.units) {
+    if (elect_one_sync()) {
+      const SubProblem& sp = p.sub[0];
+      const int nkb = sp.rcount * sp.scount;
+      uint8_t* res = pipe + C::STAGE * C::STAGES;
+      mbar_arrive_expect_tx(bfull, static_cast<uint32_t>(nkb * C::B_BYTES));
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int jr = kb / sp.scount;
+        const int js = kb - jr * sp.scount;
+        const int r = sp.r0 + jr * sp.rstep;
+        const int sc_ = sp.s0 + js * sp.sstep;
+        // K-major (fprop) and MN-major (dgrad) filter maps both start the
+        // single column tile and reduction block at coordinate 0
+        tma_load_4d(res + kb * C::B_BYTES, &p.mapB, bfull, 0, sc_, r, 0);
+      }
+    }
+    __syncwarp();
+    b_issued = true;
+  }
+  uint8_t* stage = pipe + pid * C::STAGE;
+  uint32_t phase = 0;
+  bool issued = false;
+  int k = 0;  // this CTA's unit count so far
+  UnitWalk uw;
+  for (walk_begin(p, sc, uw); uw.u < sc.units; walk_next(p, sc, uw), ++k) {
+    if (k % C::NP != pid) continue;
+    const Work w = walk_work(p, sc, uw);
+    if (!__all_sync(0xffffffffu, mbar_wait(&empty[pid], phase ^ 1u, abort_flag, timeout))) {
+      if (lane == 0) report_failure(p, abort_flag, DEVERR_PRODUCER_WAIT);
+      break;
+    }
+    if (elect_one_sync()) {
+      const int m0 = w.tile_m * kBlockM;
+      const int n = m0 / per_img;
+      const int row0 = (m0 - n * per_img) / Wt;
+      mbar_arrive_expect_tx(&full[pid], bytes);
+      tma_load_4d(stage, map, &full[pid], 0, lower_w, lower_h + row0, n);
+    }
+    __syncwarp();
+    issued = true;
+    phase ^= 1u;
+  }
+  // every copy this producer issued must land before the CTA exits
+  if (issued && !mbar_wait(&full[pid], phase ^ 1u, nullptr, timeout) && lane == 0)
+    report_failure(p, abort_flag, DEVERR_TEARDOWN_WAIT);
+  if (b_issued && !mbar_wait(bfull, 0u, nullptr, timeout) && lane == 0)
+    report_failure(p, abort_flag, DEVERR_TEARDOWN_WAIT);
+}
+
+// MMA issuer `issuer` (0 or 1) of a halo plan: for each unit, the blocks of
+// its sequence parity, each four MMAs reading the halo at the block's tap
+// offset and the block's resident filter rows; one commit per halo frees
+// its share of the stage.
+__device__ __forceinline__ void run_mma_halo(const ConvGemmParams& p, uint8_t* pipe,
+                                             uint64_t* full, uint64_t* empty, uint64_t* tfull,
+                                             uint64_t* tempty, uint64_t* done_bar,
+                                             uint64_t* bfull, uint32_t tmem_base,
+                                             volatile int* abort_flag, int issuer, int lane) {
+  using C = HaloCfg;
+  const Sched sc = load_sched<false>(p);
+  const unsigned long long timeout = p.timeout_ns;
+  const SubProblem& sp = p.sub[0];
+  const int Wt = sp.Ws;
+  const int scount = sp.scount;
+  const int nk = sp.rcount * sp.scount;
+  const int offh0 = sp.offh0, doffh = sp.doffh, offw0 = sp.offw0, doffw = sp.doffw;
+  const bool b_mn = p.b_src == SRC_W_MN;
+  const uint32_t idesc = p.idesc;
+  const int num_acc = p.num_acc;
+  const uint32_t pipe_addr = smem_u32(pipe);
+  const uint64_t a0 = make_smem_desc(pipe_addr, 16, 1024);
+  const uint64_t b0 = make_smem_desc(pipe_addr + C::STAGE * C::STAGES, b_mn ? 8192 : 16, 1024);
+  const uint64_t ak = 32 / 16;
+  const uint64_t bk = b_mn ? 2048 / 16 : 32 / 16;
+  const int buf_shift = p.epi_groups == 2 ? 2 : 1;
+  const int buf_mask = (1 << buf_shift) - 1;
+  bool ok = true;
+  if (unit_first(sc) < sc.units) {
+    if (!__all_sync(0xffffffffu, mbar_wait(bfull, 0u, abort_flag, timeout))) {
+      if (lane == 0) report_failure(p, abort_flag, DEVERR_MMA_FULL_WAIT);
+      ok = false;
+    }
+    tc_fence_after_sync();
+  }
+  int st = 0;           // halo stage of the next unit
+  uint32_t ph = 0;
+  int qpar = 0;         // parity of the unit's first block in the CTA-wide sequence
+  int local = 0;
+  UnitWalk uw;
+  for (walk_begin(p, sc, uw); ok && uw.u < sc.units; walk_next(p, sc, uw)) {
+    const int buf = local & buf_mask;
+    const uint32_t tph = static_cast<uint32_t>(local >> buf_shift) & 1u;
+    if (!__all_sync(0xffffffffu, mbar_wait(&tempty[buf], tph ^ 1u, abort_flag, timeout))) {
+      if (lane == 0) report_failure(p, abort_flag, DEVERR_MMA_TMEM_WAIT);
+      break;
+    }
+    tc_fence_after_sync();
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[st], ph, abort_flag, timeout))) {
+      if (lane == 0) report_failure(p, abort_flag, DEVERR_MMA_FULL_WAIT);
+      break;
+    }
+    tc_fence_after_sync();
+    const uint32_t d = tmem_base + static_cast<uint32_t>((buf * num_acc + issuer) * 64);
+    // The whole halo is in place, so one lane issues all of this issuer's
+    // blocks back to back; the tap position (jr, js) advances by two blocks
+    // at a time without a division.
+    if (elect_one_sync()) {
+      int rel = issuer ^ qpar;
+      int jr = 0, js = rel;
+      while (js >= scount) {
+        js -= scount;
+        ++jr;
+      }
+      uint64_t ad_unit = a0 + (static_cast<uint32_t>(st * C::STAGE) >> 4);
+      uint32_t acc = 0u;
+      for (; rel < nk; rel += 2) {
+        const int row = (offh0 + jr * doffh) * Wt + offw0 + js * doffw;
+        const uint64_t ad = ad_unit + ((static_cast<uint32_t>(row) * 128u) >> 4);
+        const uint64_t bd = b0 + static_cast<uint64_t>(rel) * (C::B_BYTES / 16);
+        mma_issue<false>(d, ad, bd, idesc, acc);
+        mma_issue<false>(d, ad + ak, bd + bk, idesc, 1u);
+        mma_issue<false>(d, ad + 2 * ak, bd + 2 * bk, idesc, 1u);
+        mma_issue<false>(d, ad + 3 * ak, bd + 3 * bk, idesc, 1u);
+        acc = 1u;
+        js += 2;
+        while (js >= scount) {
+          js -= scount;
+          ++jr;
+        }
+      }
+      mma_commit<false>(&empty[st]);   // this issuer's reads of the halo
+      mma_commit<false>(&tfull[buf]);  // this issuer's accumulator
+    }
+    __syncwarp();
+    qpar ^= nk & 1;
+    if (++st == C::STAGES) {
+      st = 0;
+      ph ^= 1u;
+    }
+    ++local;
+  }
+  // Every MMA issued must complete before TMEM is released.
+  if (elect_one_sync()) mma_commit<false>(done_bar);
+  __syncwarp();
+  if (!__all_sync(0xffffffffu, mbar_wait(done_bar, 0, nullptr, timeout)) && lane == 0)
+    report_failure(p, abort_flag, DEVERR_TEARDOWN_WAIT);
+}
+
+// The halo kernel: the same roles and epilogue (16-bit stores) as
+// conv_gemm_kernel<64, false, false, false, true>, with the halo producers
+// and issuers above (a template, so that only the translation unit that
+// launches it compiles it; BN is 64).
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    conv_gemm_halo_kernel(const __grid_constant__ ConvGemmParams p) {
+  static_assert(BN == 64, "halo plans use 64-wide tiles");
+  using C = HaloCfg;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  if (static_cast<int>(smem - smem_raw) + C::USED > C::SMEM) {
+    if (threadIdx.x == 0) atomicCAS(p.status, 0u, static_cast<unsigned int>(DEVERR_SMEM_LAYOUT));
+    return;
+  }
+  uint8_t* pipe = smem;
+  uint8_t* stage_buf = smem + C::PIPE;
+  uint32_t* bias_s = reinterpret_cast<uint32_t*>(smem + C::PIPE + C::EPI_STAGE);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::PIPE + C::EPI_STAGE + kBiasBytes);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* tfull = empty + C::STAGES;
+  uint64_t* tempty = tfull + 4;
+  uint64_t* done_bar = tempty + 4;
+  uint64_t* bfull = done_bar + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bfull + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int nbuf = p.epi_groups == 2 ? 4 : 2;
+  const uint32_t tmem_cols = tmem_cols_for(static_cast<uint32_t>(nbuf * p.num_acc * 64));
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], C::NI);  // both issuers read every halo
+    }
+    const int epi_warps = p.epi_groups == 2 ? kEpiWarps / 2 : kEpiWarps;
+    for (int b = 0; b < 4; ++b) {
+      mbar_init(&tfull[b], C::NI);
+      mbar_init(&tempty[b], epi_warps);
+    }
+    mbar_init(&done_bar[0], 1);
+    mbar_init(&done_bar[1], 1);
+    mbar_init(bfull, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (p.bias_cached) {
+    for (int i = threadIdx.x; i < p.N_gemm; i += blockDim.x) {
+      const uint16_t b = static_cast<const uint16_t*>(p.bias)[i];
+      bias_s[i] = __float_as_uint(p.out_bf16 ? __bfloat162float(__ushort_as_bfloat16(b))
+                                             : __half2float(__ushort_as_half(b)));
+    }
+  }
+  if (warp == kMmaWarp0) tmem_alloc(tmem_slot, tmem_cols);
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp < 4) {
+    setmaxnreg_dec<kRegsLow>();
+    if (warp < C::NP) {
+      if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&p.mapA[0]);
+        tma_prefetch_map(&p.mapB);
+        if (p.use_tma_store) tma_prefetch_map(&p.mapY);
+      }
+      __syncwarp();
+      run_producer_halo(p, pipe, full, empty, bfull, abort_flag, warp, lane);
+    }
+  } else if (warp >= kMmaWarp0) {
+    setmaxnreg_dec<kRegsLow>();
+    if (warp < kMmaWarp0 + C::NI)
+      run_mma_halo(p, pipe, full, empty, tfull, tempty, &done_bar[warp - kMmaWarp0], bfull,
+                   tmem_base, abort_flag, warp - kMmaWarp0, lane);
+  } else {
+    setmaxnreg_inc<kRegsEpi>();
+    run_epilogue<BN, false, false, true>(p, tfull, tempty, tmem_base, abort_flag, warp, stage_buf,
+                                         bias_s);
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp0) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, tmem_cols);
+  }
+}
+
 // The register split assumes the kernel was compiled at exactly
 // kLaunchRegs per thread (the pool the warpgroups divide); any other count
 // is refused before launch instead of risking an inc that cannot complete.

@@ -14,6 +14,8 @@ namespace igc {
 constexpr int kBlockM = 128;
 constexpr int kBlockK = 64;
 constexpr int kBiasCacheBytes = 2048;  // bias vectors up to this size are staged in shared memory
+constexpr int kHaloTaps = 9;           // halo plans: filter taps kept resident in shared memory
+constexpr int kHaloRows = 320;         // halo plans: pixel rows of 128 bytes per halo stage
 constexpr int kMaxSub = 16;      // dgrad stride decomposition: stride_h * stride_w <= 16
 constexpr int kThreads = 512;    // warps 0-3 TMA producers, 4-11 epilogue, 12-13 MMA issuers
 
@@ -87,6 +89,10 @@ struct ConvGemmParams {
   uint32_t mapA_valid;        // bit i: mapA[i] holds an encoded map
   int use_tma_store;          // output tile rows are contiguous: store them with TMA
   int general_epilogue;       // 1: 16-bit store plans run on the kernels with every epilogue
+  int halo;                   // 1: halo plan (conv_gemm_halo_kernel): mapA[0] is a tiled map of
+                              // the input, box (64 channels, Ws pixels, halo rows, 1); sub[0]
+                              // is the stride-1 plan on a grid Ws = 32/64/128 columns wide
+  int halo_bytes;             // bytes one halo copy lands (the whole box)
   int store_5d;               // strided dgrad: mapY is dX viewed as (c, w % sw, w / sw, h % sh,
                               // n * H / sh + h / sh), a residue class's grid row is one
                               // (h % sh, row) line and each 32-row box lies inside one
@@ -157,6 +163,8 @@ cudaError_t launch_conv_gemm(const ConvGemmParams& p, int block_n, int grid, cud
 // The same launch on the kernels whose epilogue holds only the 16-bit store
 // path (a plan with EPI_STORE, 16-bit outputs and no 3D operands).
 cudaError_t launch_conv_gemm_s16(const ConvGemmParams& p, int block_n, int grid, cudaStream_t s);
+// The halo kernel (a plan with p.halo set: 64-wide tiles, 16-bit stores).
+cudaError_t launch_conv_gemm_halo(const ConvGemmParams& p, int grid, cudaStream_t s);
 // Clusters of two CTAs of the kernel with this tile width that fit at once.
 int conv_gemm_pair_capacity(int block_n);
 size_t conv_gemm_smem_bytes(int block_n);

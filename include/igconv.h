@@ -610,6 +610,15 @@ IGCONV_API const char *igconv_status_string(igconv_status_t status);
  *                             only that store path (the built-in choice);
  *                             1: on the kernels that carry every epilogue.
  *                             Results are bit-identical.
+ *   IGCONV_TUNE_HALO          stride-1 fprop and dgrad with 64 output
+ *                             channels, one 64-channel reduction block and
+ *                             2..9 filter taps: 0 reads each tile's input
+ *                             rows once (a halo) for all its taps (the
+ *                             built-in choice where the output width fits a
+ *                             grid of 32, 64 or 128 columns and the output
+ *                             height a multiple of 128 / that width); 1 never
+ *                             (one im2col copy per tap).  Results are
+ *                             bit-identical.
  * Returns INVALID_ARG for an unknown key or value. */
 typedef enum {
     IGCONV_TUNE_WGRAD_SPLITS = 1,
@@ -622,7 +631,8 @@ typedef enum {
     IGCONV_TUNE_RASTER = 8,
     IGCONV_TUNE_RESIDENT_FILTER = 9,
     IGCONV_TUNE_DGRAD_ROWS = 10,
-    IGCONV_TUNE_EPILOGUE_KERNEL = 11
+    IGCONV_TUNE_EPILOGUE_KERNEL = 11,
+    IGCONV_TUNE_HALO = 12
 } igconv_tune_key_t;
 IGCONV_API igconv_status_t igconv_set_tuning(igconv_tune_key_t key, int value);
 

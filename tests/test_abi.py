@@ -181,6 +181,9 @@ def test_tuning_keys(igc):
     assert lib.igconv_set_tuning(igc.TUNE_EPILOGUE_KERNEL, 2) == 1
     assert lib.igconv_set_tuning(igc.TUNE_EPILOGUE_KERNEL, 1) == 0
     assert lib.igconv_set_tuning(igc.TUNE_EPILOGUE_KERNEL, 0) == 0
+    assert lib.igconv_set_tuning(igc.TUNE_HALO, 2) == 1
+    assert lib.igconv_set_tuning(igc.TUNE_HALO, 1) == 0
+    assert lib.igconv_set_tuning(igc.TUNE_HALO, 0) == 0
 
 
 def test_grouped_reject_invalid(igc):
