@@ -239,7 +239,8 @@ void set_out_map_16(ConvGemmParams& p, void* base, long long rows, long long col
 // and by halo plans (sh = sw = 1).
 void set_out_map_lines_5d(ConvGemmParams& p, void* out, int N, int H, int W, int C, int sh,
                           int sw, int bf16, int bn, int kblocks_per_tile) {
-  const bool wide = bn >= 128 && kblocks_per_tile <= 2;
+  // halo plans store 64-column boxes (one accumulator: two chunks per box)
+  const bool wide = (bn >= 128 && kblocks_per_tile <= 2) || p.one_issuer;
   const cuuint64_t px = static_cast<cuuint64_t>(C) * 2;
   const cuuint64_t dims[5] = {static_cast<cuuint64_t>(C), static_cast<cuuint64_t>(sw),
                               static_cast<cuuint64_t>(W / sw), static_cast<cuuint64_t>(sh),
@@ -314,6 +315,8 @@ bool try_halo_plan(ConvGemmParams& p, int bn, const void* in, int N, int Hin, in
   p.units = s.tiles_m;
   p.halo = 1;
   p.halo_bytes = hr * wt * 128;
+  p.one_issuer = 1;
+  p.num_acc = 1;
   p.res_b = 0;
   return true;
 }

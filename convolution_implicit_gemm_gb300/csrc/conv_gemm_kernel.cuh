@@ -1023,6 +1023,7 @@ struct EpiCtx {
   unsigned long long timeout;
   int use_tma;
   int store5;           // TMA stores through the 5D strided-dgrad view (see OutAt)
+  int one_issuer;       // each unit is issued by one issuer into one accumulator
   int box64;            // 16-bit output boxes of 64 columns (128-byte swizzle)
   int ws_rows_per_split;   // M_pad (wgrad)
   int int_acc;             // accumulators hold exact integers: sum and store them as int32
@@ -1059,6 +1060,7 @@ __device__ __forceinline__ void run_epilogue(const ConvGemmParams& p, uint64_t* 
   e.timeout = p.timeout_ns;
   e.use_tma = p.use_tma_store;
   e.store5 = p.use_tma_store && p.store_5d && e.sc.epi == EPI_STORE;
+  e.one_issuer = p.one_issuer;
   e.box64 = p.use_tma_store && p.store_box64 && e.sc.epi == EPI_STORE;
   e.ws_rows_per_split = p.tiles_m_total * kBlockM;
   e.int_acc = S16 ? 0 : p.int_acc;
@@ -1104,8 +1106,10 @@ __device__ __forceinline__ void run_epilogue(const ConvGemmParams& p, uint64_t* 
     const int q0 = qseq;
     if (has_acc) qseq += nk;
     // which of the first NI accumulators hold blocks (NI == 2: at least one)
-    const bool use1 = NI >= 2 && acc_used(e.kb_per_acc, 1, NI, nk, q0);
-    const uint32_t lone = (NI >= 2 && !acc_used(e.kb_per_acc, 0, NI, nk, q0)) ? BN : 0u;
+    // (a unit issued by a single issuer has one accumulator, at offset 0)
+    const bool use1 = NI >= 2 && !e.one_issuer && acc_used(e.kb_per_acc, 1, NI, nk, q0);
+    const uint32_t lone =
+        (NI >= 2 && !e.one_issuer && !acc_used(e.kb_per_acc, 0, NI, nk, q0)) ? BN : 0u;
     const int buf = local & buf_mask;
     const uint32_t tph = static_cast<uint32_t>(local >> buf_shift) & 1u;
     if (groups == 2 && ((has_acc ? local : plain) & 1) != group) {
@@ -1252,8 +1256,8 @@ __device__ __forceinline__ void run_epilogue(const ConvGemmParams& p, uint64_t* 
       // bias: chunks go in pairs, one TMEM round trip and one store per pair
       // (with 32-column boxes the pair's extra live registers cost more than
       // the saved round trip).
-      const bool pair1 = NI == 1 && e.box64 && e.num_acc == 1 && has_acc && e.beta == 0.0f &&
-                         (e.bias == nullptr || bias_cached);
+      const bool pair1 = (NI == 1 || e.one_issuer) && e.box64 && e.num_acc == 1 && has_acc &&
+                         e.beta == 0.0f && (e.bias == nullptr || bias_cached);
 #pragma unroll 1
       for (int j = j0; j < j1; ++j) {
         const int n0 = w.tile_n * BN + j * 32;
@@ -1681,9 +1685,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 // chunk index XOR address bits 7-9), for the TMA that writes the halo and
 // the MMA that reads it alike, so the base-offset field stays zero (checked
 // on the GPU: with the field set to the start's row within the pattern the
-// products were wrong, with it zero exact).  Both issuers read every halo
-// (each takes the blocks of its sequence parity), so a halo stage is free
-// once both have committed.  Junk columns (grid column >= the output width)
+// products were wrong, with it zero exact).  The two issuers take alternate
+// units whole (p.one_issuer), each into the unit's single accumulator, so
+// the epilogue reads one accumulator and stores 64-column boxes; without
+// one_issuer both read every halo (each the blocks of its sequence parity)
+// and a stage is free once both have committed.  Junk columns (grid column >= the output width)
 // read neighbouring pixels; the epilogue drops them (ws_valid, and the
 // output map clips them).
 // ---------------------------------------------------------------------------
@@ -1803,12 +1809,29 @@ __device__ __forceinline__ void run_mma_halo(const ConvGemmParams& p, uint8_t* p
     }
     tc_fence_after_sync();
   }
+  const bool one = p.one_issuer != 0;
   int st = 0;           // halo stage of the next unit
   uint32_t ph = 0;
   int qpar = 0;         // parity of the unit's first block in the CTA-wide sequence
   int local = 0;
   UnitWalk uw;
   for (walk_begin(p, sc, uw); ok && uw.u < sc.units; walk_next(p, sc, uw)) {
+    if (one && (local & 1) != issuer) {
+      // The other issuer's unit.  With three stages consecutive fills of a
+      // stage belong to different issuers, so this issuer still waits for
+      // the fill to land: having seen every fill of a stage in order, its
+      // parity wait on the next one cannot be passed by the phase before.
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[st], ph, abort_flag, timeout))) {
+        if (lane == 0) report_failure(p, abort_flag, DEVERR_MMA_FULL_WAIT);
+        break;
+      }
+      if (++st == C::STAGES) {
+        st = 0;
+        ph ^= 1u;
+      }
+      ++local;
+      continue;
+    }
     const int buf = local & buf_mask;
     const uint32_t tph = static_cast<uint32_t>(local >> buf_shift) & 1u;
     if (!__all_sync(0xffffffffu, mbar_wait(&tempty[buf], tph ^ 1u, abort_flag, timeout))) {
@@ -1821,12 +1844,15 @@ __device__ __forceinline__ void run_mma_halo(const ConvGemmParams& p, uint8_t* p
       break;
     }
     tc_fence_after_sync();
-    const uint32_t d = tmem_base + static_cast<uint32_t>((buf * num_acc + issuer) * 64);
+    const uint32_t d =
+        tmem_base + static_cast<uint32_t>((buf * num_acc + (one ? 0 : issuer)) * 64);
     // The whole halo is in place, so one lane issues all of this issuer's
-    // blocks back to back; the tap position (jr, js) advances by two blocks
-    // at a time without a division.
+    // blocks back to back (every block of the unit with one issuer per unit,
+    // else those of its sequence parity); the tap position (jr, js) advances
+    // without a division.
     if (elect_one_sync()) {
-      int rel = issuer ^ qpar;
+      const int step = one ? 1 : 2;
+      int rel = one ? 0 : issuer ^ qpar;
       int jr = 0, js = rel;
       while (js >= scount) {
         js -= scount;
@@ -1834,7 +1860,7 @@ __device__ __forceinline__ void run_mma_halo(const ConvGemmParams& p, uint8_t* p
       }
       uint64_t ad_unit = a0 + (static_cast<uint32_t>(st * C::STAGE) >> 4);
       uint32_t acc = 0u;
-      for (; rel < nk; rel += 2) {
+      for (; rel < nk; rel += step) {
         const int row = (offh0 + jr * doffh) * Wt + offw0 + js * doffw;
         const uint64_t ad = ad_unit + ((static_cast<uint32_t>(row) * 128u) >> 4);
         const uint64_t bd = b0 + static_cast<uint64_t>(rel) * (C::B_BYTES / 16);
@@ -1843,7 +1869,7 @@ __device__ __forceinline__ void run_mma_halo(const ConvGemmParams& p, uint8_t* p
         mma_issue<false>(d, ad + 2 * ak, bd + 2 * bk, idesc, 1u);
         mma_issue<false>(d, ad + 3 * ak, bd + 3 * bk, idesc, 1u);
         acc = 1u;
-        js += 2;
+        js += step;
         while (js >= scount) {
           js -= scount;
           ++jr;
@@ -1901,13 +1927,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_cols = tmem_cols_for(static_cast<uint32_t>(nbuf * p.num_acc * 64));
 
   if (threadIdx.x == 0) {
+    // one issuer per unit (one_issuer): each halo and accumulator has one
+    // consumer / producer; otherwise both issuers read every halo
+    const int consumers = p.one_issuer ? 1 : C::NI;
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], C::NI);  // both issuers read every halo
+      mbar_init(&empty[s], consumers);
     }
     const int epi_warps = p.epi_groups == 2 ? kEpiWarps / 2 : kEpiWarps;
     for (int b = 0; b < 4; ++b) {
-      mbar_init(&tfull[b], C::NI);
+      mbar_init(&tfull[b], consumers);
       mbar_init(&tempty[b], epi_warps);
     }
     mbar_init(&done_bar[0], 1);

@@ -571,8 +571,9 @@ IGCONV_API const char *igconv_status_string(igconv_status_t status);
  *                             wgrad partials) run their epilogue as two
  *                             groups of four warps taking alternate tiles,
  *                             with four TMEM buffers; 1: one group of eight
- *                             warps per tile, two buffers.  Results are
- *                             bit-identical.
+ *                             warps per tile, two buffers (not for halo
+ *                             plans, see IGCONV_TUNE_HALO, which always run
+ *                             two groups).  Results are bit-identical.
  *   IGCONV_TUNE_CONV_SPLITS   split-K of conv2d_fprop_ws / conv2d_dgrad_ws
  *                             (when given a workspace): 0 or 1 never (the
  *                             built-in choice), n >= 2 always n (at most 16,
@@ -617,8 +618,11 @@ IGCONV_API const char *igconv_status_string(igconv_status_t status);
  *                             built-in choice where the output width fits a
  *                             grid of 32, 64 or 128 columns and the output
  *                             height a multiple of 128 / that width); 1 never
- *                             (one im2col copy per tap).  Results are
- *                             bit-identical.
+ *                             (one im2col copy per tap).  The halo plan adds
+ *                             a tile's taps in order into one fp32
+ *                             accumulator, the per-tap plan alternates them
+ *                             between two, so on non-integer data the two
+ *                             round differently (each deterministically).
  * Returns INVALID_ARG for an unknown key or value. */
 typedef enum {
     IGCONV_TUNE_WGRAD_SPLITS = 1,

