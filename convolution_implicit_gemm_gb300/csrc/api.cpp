@@ -48,7 +48,8 @@ PFN_encodeTiled g_encode_tiled = nullptr;
 PFN_encodeIm2col g_encode_im2col = nullptr;
 std::atomic<int> g_tune_splits{0}, g_tune_bn{0}, g_tune_max_ctas{0}, g_tune_no_pairs{0},
     g_tune_epi_groups{0}, g_tune_conv_splits{0}, g_tune_few_channels{0}, g_tune_raster{0},
-    g_tune_resident_b{0}, g_tune_dgrad_rows{0}, g_tune_general_epi{0}, g_tune_halo{0};
+    g_tune_resident_b{0}, g_tune_dgrad_rows{0}, g_tune_general_epi{0}, g_tune_halo{0},
+    g_tune_one_issuer{0};
 
 igconv_status_t device_state(DeviceState** out) {
   int dev = 0;
@@ -214,6 +215,23 @@ bool encode_out_2d(CUtensorMap* map, void* base, CUtensorMapDataType dt, int esi
   return r == CUDA_SUCCESS;
 }
 
+// 64-wide 16-bit-store plans whose units hold at most four reduction blocks
+// (1x1 layers over up to 256 channels, the packed stem, strided dgrad's
+// residue classes) are bound by their epilogue: there the two MMA issuers
+// take alternate units whole, each into the unit's one accumulator
+// (num_acc = 1), so the epilogue reads one accumulator and stores 64-column
+// boxes (see run_mma).  Call before the output map is encoded; knob
+// IGCONV_TUNE_ONE_ISSUER = 1 keeps two accumulators per unit.
+void choose_one_issuer(ConvGemmParams& p, int bn) {
+  if (g_tune_one_issuer.load() == 1 || bn != 64 || p.pair || p.halo) return;
+  int kb = 0;
+  for (int i = 0; i < p.nsub; ++i)
+    kb = std::max(kb, p.sub[i].rcount * p.sub[i].scount * p.cblocks);
+  if (kb < 1 || kb > 4) return;
+  p.one_issuer = 1;
+  p.num_acc = 1;
+}
+
 // Output map for a 16-bit [rows x cols] output written by TMA stores.  Boxes
 // are 32 rows x 32 columns, double-buffered per epilogue warp; a GEMM whose
 // reduction is at most two blocks per tile is bound by its epilogue, and
@@ -223,7 +241,8 @@ bool encode_out_2d(CUtensorMap* map, void* base, CUtensorMapDataType dt, int esi
 // buffer they allow costs a few percent.
 void set_out_map_16(ConvGemmParams& p, void* base, long long rows, long long cols, int bf16,
                     int bn, int kblocks_per_tile) {
-  const bool wide = bn >= 128 && kblocks_per_tile <= 2;
+  // (one accumulator per 64-wide unit: two chunks per 64-column box)
+  const bool wide = (bn >= 128 && kblocks_per_tile <= 2) || p.one_issuer;
   p.use_tma_store = encode_out_2d(&p.mapY, base, tma_dtype(bf16), 2, rows, cols, wide ? 64 : 32,
                                   wide ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B)
                         ? 1
@@ -1474,6 +1493,10 @@ igconv_status_t igconv_set_tuning(igconv_tune_key_t key, int value) {
       if (value < 0 || value > 1) return IGCONV_ERR_INVALID_ARG;
       g_tune_halo.store(value);
       return IGCONV_OK;
+    case IGCONV_TUNE_ONE_ISSUER:
+      if (value < 0 || value > 1) return IGCONV_ERR_INVALID_ARG;
+      g_tune_one_issuer.store(value);
+      return IGCONV_OK;
   }
   return IGCONV_ERR_INVALID_ARG;
 }
@@ -1602,6 +1625,7 @@ igconv_status_t conv2d_fprop_ws(const igconv_problem_t* prob, igconv_dtype_t dty
                          p.sub[0].rcount * p.sub[0].scount * p.cblocks);
   } else {
     // output tile rows are consecutive pixels: store them with TMA
+    if (splits == 1) choose_one_issuer(p, bn);
     set_out_map_16(p, Y, static_cast<long long>(prob->N) * P * Q, prob->K, bf16, bn,
                    p.sub[0].rcount * p.sub[0].scount * p.cblocks);
   }
@@ -1634,6 +1658,7 @@ static igconv_status_t launch_dgrad_plan(ConvGemmParams& p, int bn, const igconv
                                          int bf16, const DeviceState* dev, cudaStream_t stream) {
   p.epi = EPI_STORE;
   p.out = dX;
+  choose_one_issuer(p, bn);  // whichever way the rows are stored
   if (p.halo) {
     // halo plan: grid rows are whole dX rows
     set_out_map_lines_5d(p, dX, prob->N, prob->H, prob->W, prob->C, 1, 1, bf16, bn,

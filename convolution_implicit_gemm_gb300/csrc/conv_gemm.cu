@@ -64,8 +64,9 @@ cudaError_t launch_conv_gemm(const ConvGemmParams& p_in, int block_n, int grid, 
   ConvGemmParams p = p_in;
   const bool fits = block_n == 64 && !p.pair && p.epi != EPI_PARTIAL && 4 * p.num_acc * 64 <= 512;
   p.epi_groups = (fits && p.epi_groups != 1) ? 2 : 1;
-  // halo plans store 64-column boxes, whole tiles per warp: two groups always
-  if (p.halo) p.epi_groups = 2;
+  // halo and one-issuer plans store 64-column boxes, whole tile rows per
+  // warp: two groups always
+  if (p.halo || (p.one_issuer && block_n == 64)) p.epi_groups = 2;
   // Resident filter (p.res_b set by the planner when allowed): 64-wide tiles
   // of a single column tile and one sub-problem, whole-tile units, the
   // filter a plain tiled operand, at most kResBlocks blocks per unit.

@@ -741,11 +741,40 @@ __device__ __forceinline__ void run_mma(const ConvGemmParams& p, uint8_t* pipe, 
     }
     tc_fence_after_sync();
   }
+  // One issuer per unit (p.one_issuer, 64-wide plans of short reductions):
+  // the issuers take alternate units whole, each into the unit's one
+  // accumulator.  A stage then serves both issuers over time, so the issuer
+  // also waits, in order, for the fills of the units it skips: having seen
+  // every fill of every stage, its parity wait on a stage cannot be passed by
+  // the phase before.
+  const bool one = NI == 2 && p.one_issuer != 0;
+  const int rstep = one ? 1 : NI;
   UnitWalk uw;
   for (walk_begin(p, sc, uw); ok && uw.u < sc.units; walk_next(p, sc, uw)) {
     const Work w = walk_work(p, sc, uw);
     const int nk = w.kb1 - w.kb0;
     if (nk <= 0) continue;  // no reduction: the epilogue writes beta*Cin alone
+    if (one && (local & 1) != issuer) {
+      int st = stage;
+      uint32_t ph = phase;
+      for (int rel = 0; rel < nk; ++rel) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&full[st], ph, abort_flag, timeout))) {
+          if (lane == 0) report_failure(p, abort_flag, DEVERR_MMA_FULL_WAIT);
+          ok = false;
+          break;
+        }
+        if (++st == STAGES) {
+          st = 0;
+          ph ^= 1u;
+        }
+      }
+      const int adv = stage + nk;
+      const int wraps = adv / STAGES;
+      stage = adv - wraps * STAGES;
+      phase ^= static_cast<uint32_t>(wraps & 1);
+      ++local;
+      continue;
+    }
     const int buf = local & buf_mask;
     const uint32_t tph = static_cast<uint32_t>(local >> buf_shift) & 1u;
     if (!__all_sync(0xffffffffu, mbar_wait(&tempty[buf], tph ^ 1u, abort_flag, timeout))) {
@@ -753,8 +782,8 @@ __device__ __forceinline__ void run_mma(const ConvGemmParams& p, uint8_t* pipe, 
       break;
     }
     tc_fence_after_sync();
-    uint32_t d = tmem_base + static_cast<uint32_t>((buf * num_acc + issuer) * BN);
-    const int r0 = first_rel(issuer, NI, stage);  // stage has the parity of q0
+    uint32_t d = tmem_base + static_cast<uint32_t>((buf * num_acc + (one ? 0 : issuer)) * BN);
+    const int r0 = one ? 0 : first_rel(issuer, NI, stage);  // stage has the parity of q0
     int st = stage + r0;
     uint32_t ph = phase;
     if (st >= STAGES) {
@@ -763,7 +792,7 @@ __device__ __forceinline__ void run_mma(const ConvGemmParams& p, uint8_t* pipe, 
     }
     int left = kb_per_acc;   // blocks still to add into the current accumulator
     uint32_t acc = 0u;       // 0: the next MMA overwrites the accumulator
-    for (int rel = r0; rel < nk; rel += NI) {
+    for (int rel = r0; rel < nk; rel += rstep) {
       if (!__all_sync(0xffffffffu, mbar_wait(&full[st], ph, abort_flag, timeout))) {
         if (lane == 0) report_failure(p, abort_flag, DEVERR_MMA_FULL_WAIT);
         ok = false;
@@ -787,7 +816,7 @@ __device__ __forceinline__ void run_mma(const ConvGemmParams& p, uint8_t* pipe, 
         d += static_cast<uint32_t>(NI * BN);
         acc = 0u;
       }
-      st += NI;
+      st += rstep;
       if (st >= STAGES) {
         st -= STAGES;
         ph ^= 1u;
@@ -1581,7 +1610,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the even CTA's TMEM-empty barriers count both CTAs' epilogues
     const int epi_warps = p.epi_groups == 2 ? kEpiWarps / 2 : kEpiWarps;
     for (int b = 0; b < 4; ++b) {
-      mbar_init(&tfull[b], C::NI);
+      mbar_init(&tfull[b], p.one_issuer ? 1 : C::NI);  // one issuer per unit, or all
       mbar_init(&tempty[b], PAIR ? 2 * epi_warps : epi_warps);
     }
     mbar_init(&done_bar[0], 1);

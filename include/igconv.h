@@ -623,6 +623,15 @@ IGCONV_API const char *igconv_status_string(igconv_status_t status);
  *                             accumulator, the per-tap plan alternates them
  *                             between two, so on non-integer data the two
  *                             round differently (each deterministically).
+ *   IGCONV_TUNE_ONE_ISSUER    fprop / dgrad with 64-wide tiles of at most
+ *                             four reduction blocks (1x1 layers, the packed
+ *                             stem, strided dgrad): 0 each tile is issued by
+ *                             one of the two MMA issuers into one
+ *                             accumulator (the built-in choice); 1 the
+ *                             issuers alternate blocks into two
+ *                             accumulators.  The two add the blocks in
+ *                             different orders: exact alike on integer data,
+ *                             each deterministic otherwise.
  * Returns INVALID_ARG for an unknown key or value. */
 typedef enum {
     IGCONV_TUNE_WGRAD_SPLITS = 1,
@@ -636,7 +645,8 @@ typedef enum {
     IGCONV_TUNE_RESIDENT_FILTER = 9,
     IGCONV_TUNE_DGRAD_ROWS = 10,
     IGCONV_TUNE_EPILOGUE_KERNEL = 11,
-    IGCONV_TUNE_HALO = 12
+    IGCONV_TUNE_HALO = 12,
+    IGCONV_TUNE_ONE_ISSUER = 13
 } igconv_tune_key_t;
 IGCONV_API igconv_status_t igconv_set_tuning(igconv_tune_key_t key, int value);
 
