@@ -278,56 +278,75 @@ __device__ __forceinline__ bool row_target(int mx, int RS, int C, int cpad, cons
   return *tap < RS && *c < C;
 }
 
-// Many splits (more than 8): each warp covers 8 rows x 64 columns with
-// 4-byte loads, so a block holds only 8 rows and the small outputs these
-// plans have still spread over enough blocks; split group g adds splits
-// g, g + G, ... in index order and the group sums are added in group order.
-template <int G>
+// Many splits (more than 8): the eight warps of a block are eight split
+// groups over the same RPW rows x 64 columns (4-byte loads, lanes along the
+// columns); group g adds splits g, g + 8, ... in index order, four splits'
+// loads in flight at a time, and the group sums are added in group order.
+// RPW (8, 4, 2 or 1) is chosen by the launcher so that the small outputs
+// these plans have still spread over at least two blocks per SM: with 8 rows
+// a 56x56 64->64 3x3 wgrad (576 x 64 outputs, 30 splits) had 72 blocks, ran
+// latency-bound at 8 % of the memory throughput and took 7.3 us.
+template <int RPW>
 __global__ void __launch_bounds__(256) wgrad_reduce_many_kernel(
     const float* __restrict__ ws, int splits, long long split_stride, int ws_ld, int rows,
     int cols, int swapped, int K, int RS, int C, int cpad, void* dW, int dw_dtype,
     const void* cin, float alpha, float beta, FewPack remap) {
-  constexpr int RG = 8 / G;    // row groups
-  constexpr int TR = 8 * RG;   // workspace rows per tile
+  constexpr int G = 8;      // split groups, one per warp
+  constexpr int TR = RPW;   // workspace rows per tile
   __shared__ float part[G][TR][65];
-  const int warp = threadIdx.x >> 5;
+  const int g = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int g = warp % G;
-  const int rg = warp / G;
   const int tiles_c = (cols + 63) / 64;
   const int tiles = ((rows + TR - 1) / TR) * tiles_c;
   for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
     const int r0 = (t / tiles_c) * TR;
     const int c0 = (t % tiles_c) * 64;
-    float acc[8][2];
+    float acc[RPW][2];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = 0.0f;
-    const int rbase = r0 + rg * 8;
-    bool rv[8], cv[2];
+    for (int i = 0; i < RPW; ++i) acc[i][0] = acc[i][1] = 0.0f;
+    bool rv[RPW], cv[2];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) rv[i] = rbase + i < rows;
+    for (int i = 0; i < RPW; ++i) rv[i] = r0 + i < rows;
     cv[0] = c0 + lane < cols;
     cv[1] = c0 + 32 + lane < cols;
-    const float* src = ws + static_cast<long long>(rbase) * ws_ld + c0 + lane;
-    for (int sp = g; sp < splits; sp += G) {
+    const float* src = ws + static_cast<long long>(r0) * ws_ld + c0 + lane;
+    auto load = [&](int sp, float (&v)[RPW][2]) {
       const float* q = src + sp * split_stride;
-      float v[8][2];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < RPW; ++i)
 #pragma unroll
         for (int h = 0; h < 2; ++h)
-          v[i][h] = (rv[i] && cv[h]) ? __ldg(q + static_cast<long long>(i) * ws_ld + 32 * h) : 0.0f;
-      }
+          v[i][h] = (rv[i] && cv[h]) ? __ldg(q + static_cast<long long>(i) * ws_ld + 32 * h)
+                                     : 0.0f;
+    };
+    auto add = [&](const float (&v)[RPW][2]) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < RPW; ++i) {
         acc[i][0] = __fadd_rn(acc[i][0], v[i][0]);
         acc[i][1] = __fadd_rn(acc[i][1], v[i][1]);
       }
+    };
+    int sp = g;
+    for (; sp + 3 * G < splits; sp += 4 * G) {
+      float v0[RPW][2], v1[RPW][2], v2[RPW][2], v3[RPW][2];
+      load(sp, v0);
+      load(sp + G, v1);
+      load(sp + 2 * G, v2);
+      load(sp + 3 * G, v3);
+      add(v0);
+      add(v1);
+      add(v2);
+      add(v3);
+    }
+    for (; sp < splits; sp += G) {
+      float v0[RPW][2];
+      load(sp, v0);
+      add(v0);
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      part[g][rg * 8 + i][lane] = acc[i][0];
-      part[g][rg * 8 + i][lane + 32] = acc[i][1];
+    for (int i = 0; i < RPW; ++i) {
+      part[g][i][lane] = acc[i][0];
+      part[g][i][lane + 32] = acc[i][1];
     }
     __syncthreads();
     for (int idx = threadIdx.x; idx < TR * 64; idx += 256) {
@@ -511,12 +530,26 @@ cudaError_t launch_wgrad_reduce(const float* ws, int splits, long long split_str
   FewPack remap{};
   if (remap_in) remap = *remap_in;  // remap.cz == 0: plain (tap, c) rows
   if (splits > 8) {
-    constexpr int TR = 8;
-    const long long tiles = static_cast<long long>((rows + TR - 1) / TR) * ((cols + 63) / 64);
+    // rows per tile: the most (of 8, 4, 2, 1) that still gives two blocks per SM
+    int sms = 148, dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long long tiles_c = (cols + 63) / 64;
+    int rpw = 8;
+    while (rpw > 1 && ((rows + rpw - 1) / rpw) * tiles_c < 2LL * sms) rpw >>= 1;
+    const long long tiles = ((rows + rpw - 1) / rpw) * tiles_c;
     const unsigned grid = static_cast<unsigned>(tiles < 16384 ? (tiles > 0 ? tiles : 1) : 16384);
-    wgrad_reduce_many_kernel<8><<<grid, 256, 0, s>>>(ws, splits, split_stride, ws_ld, rows, cols,
-                                                     swapped, K, RS, C, cpad, dW, dw_dtype, cin,
-                                                     alpha, beta, remap);
+#define IGC_REDUCE_MANY(R)                                                                       \
+  wgrad_reduce_many_kernel<R><<<grid, 256, 0, s>>>(ws, splits, split_stride, ws_ld, rows, cols,  \
+                                                   swapped, K, RS, C, cpad, dW, dw_dtype, cin,  \
+                                                   alpha, beta, remap)
+    switch (rpw) {
+      case 8: IGC_REDUCE_MANY(8); break;
+      case 4: IGC_REDUCE_MANY(4); break;
+      case 2: IGC_REDUCE_MANY(2); break;
+      default: IGC_REDUCE_MANY(1); break;
+    }
+#undef IGC_REDUCE_MANY
     return cudaGetLastError();
   }
   // every split group gets at least two splits, so two loads per row are in flight
