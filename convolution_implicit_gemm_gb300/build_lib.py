@@ -17,8 +17,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libigconv.so")
-SOURCES = ["api.cpp", "conv_gemm.cu", "conv_gemm_s16.cu", "aux_kernels.cu", "wgrad_noalloc.cu",
-           "depthwise.cu", "winograd.cu"]
+SOURCES = ["api.cpp", "conv_gemm.cu", "conv_gemm_s16.cu", "conv_wgrad_halo.cu", "aux_kernels.cu",
+           "wgrad_noalloc.cu", "depthwise.cu", "winograd.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

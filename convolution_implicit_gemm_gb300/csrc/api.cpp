@@ -49,7 +49,7 @@ PFN_encodeIm2col g_encode_im2col = nullptr;
 std::atomic<int> g_tune_splits{0}, g_tune_bn{0}, g_tune_max_ctas{0}, g_tune_no_pairs{0},
     g_tune_epi_groups{0}, g_tune_conv_splits{0}, g_tune_few_channels{0}, g_tune_raster{0},
     g_tune_resident_b{0}, g_tune_dgrad_rows{0}, g_tune_general_epi{0}, g_tune_halo{0},
-    g_tune_one_issuer{0};
+    g_tune_one_issuer{0}, g_tune_wgrad_halo{0};
 
 igconv_status_t device_state(DeviceState** out) {
   int dev = 0;
@@ -1421,6 +1421,95 @@ igconv_status_t run_wgrad(const igconv_problem_t* g, int P, int Q, const WgradPl
                                        remap));
 }
 
+// wgrad on input halos (conv_wgrad_halo.cu): stride 1, C and K at most 64,
+// 2..kHaloTaps taps.  Output positions run on a grid Wt = 32, 64 or 128
+// columns wide (the smallest that holds Q + the largest column offset), in
+// blocks of 128 positions = 128 / Wt whole output rows, so P must be a
+// multiple of 128 / Wt; each block's input halo of HR = 128 / Wt + the
+// largest row offset + 1 rows must fit kHaloRows.  One unit (CTA) per split,
+// at most one per SM, each computing every tap pair of its blocks; the
+// partial tiles are [split][pairs * 128][64] fp32.
+struct WgradHaloPlan {
+  int wt, rows, hr, blocks, splits, pairs;
+  size_t ws_bytes;
+};
+bool plan_wgrad_halo(const igconv_problem_t* pb, int P, int Q, int sm_count, WgradHaloPlan* h) {
+  if (g_tune_wgrad_halo.load() == 1) return false;
+  if (pb->stride_h != 1 || pb->stride_w != 1 || pb->C > 64 || pb->K > 64) return false;
+  const int taps = pb->R * pb->S;
+  if (taps < 2 || taps > kHaloTaps) return false;
+  const int max_h = (pb->R - 1) * pb->dil_h, max_w = (pb->S - 1) * pb->dil_w;
+  int wt = 32;
+  while (wt < Q + max_w && wt < 256) wt *= 2;
+  if (wt > 128 || wt < Q + max_w) return false;
+  h->wt = wt;
+  h->rows = kBlockM / wt;
+  h->hr = h->rows + max_h + 1;
+  if (h->hr * wt > kHaloRows || h->hr > 256 || P % h->rows != 0) return false;
+  const long long blocks = static_cast<long long>(pb->N) * (P / h->rows);
+  if (blocks < 1 || blocks > INT_MAX) return false;
+  h->blocks = static_cast<int>(blocks);
+  const int sms = sm_count > 0 ? sm_count : 148;
+  h->splits = h->blocks < sms ? h->blocks : sms;
+  h->pairs = (taps + 1) / 2;
+  h->ws_bytes = static_cast<size_t>(h->splits) * h->pairs * kBlockM * 64 * sizeof(float);
+  return true;
+}
+
+// Tiled map over an NHWC tensor, box (64 channels, bw pixels, bh rows, 1 image),
+// 128-byte swizzle; reads outside the tensor are zero.
+bool encode_nhwc_box(CUtensorMap* map, const void* base, int bf16, int N, int H, int W, int C,
+                     int bw, int bh) {
+  const cuuint64_t px = static_cast<cuuint64_t>(C) * 2;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(C), static_cast<cuuint64_t>(W),
+                              static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(N)};
+  const cuuint64_t strides[3] = {px, px * W, px * W * H};
+  const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(bw), static_cast<cuuint32_t>(bh), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return g_encode_tiled(map, tma_dtype(bf16), 4, const_cast<void*>(base), dims, strides, box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+igconv_status_t run_wgrad_halo(const igconv_problem_t* g, int P, int Q, const WgradHaloPlan& h,
+                               int bf16, const void* X, const void* dY, void* part,
+                               const DeviceState* dev, void* dW, igconv_dtype_t dw_dtype,
+                               const void* Cin, float alpha, float beta, cudaStream_t s) {
+  ConvGemmParams p;
+  init_common(p, dev);
+  SubProblem& sp = p.sub[0];
+  sp.Ws = h.wt;
+  sp.Hs = P;
+  sp.lower_h = -g->pad_h;
+  sp.lower_w = -g->pad_w;
+  sp.r0 = 0; sp.rstep = 1; sp.rcount = g->R; sp.offh0 = 0; sp.doffh = g->dil_h;
+  sp.s0 = 0; sp.sstep = 1; sp.scount = g->S; sp.offw0 = 0; sp.doffw = g->dil_w;
+  p.nsub = 1;
+  p.epi = EPI_PARTIAL;
+  p.splits = h.splits;
+  p.kblocks_total = h.blocks;
+  p.tiles_m_total = h.pairs;
+  p.halo_bytes = h.hr * h.wt * 128;
+  p.idesc = make_idesc(kBlockM, 64, bf16, 1, 1);
+  p.out = part;
+  if (!encode_nhwc_box(&p.mapA[0], X, bf16, g->N, g->H, g->W, g->C, h.wt, h.hr) ||
+      !encode_nhwc_box(&p.mapB, dY, bf16, g->N, P, Q, g->K, h.wt, h.rows) ||
+      !encode_out_2d(&p.mapY, part, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
+                     static_cast<long long>(h.splits) * h.pairs * kBlockM, 64, 16,
+                     CU_TENSOR_MAP_SWIZZLE_64B))
+    return IGCONV_ERR_UNSUPPORTED;
+  p.mapA_valid = 1u;
+  p.use_tma_store = 1;
+  if (launch_wgrad_halo(p, s) != cudaSuccess) return IGCONV_ERR_CUDA;
+  const int dwt = dw_dtype == IGCONV_F32 ? 2 : (dw_dtype == IGCONV_BF16 ? 1 : 0);
+  const int rows = h.pairs * kBlockM;
+  return from_cuda(launch_wgrad_reduce(static_cast<const float*>(part), h.splits,
+                                       static_cast<long long>(rows) * 64, 64, rows, 64, 0, g->K,
+                                       g->R * g->S, g->C, 64, dW, dwt,
+                                       beta != 0.0f ? Cin : nullptr, alpha, beta, s, nullptr));
+}
+
 }  // namespace
 
 extern "C" {
@@ -1496,6 +1585,10 @@ igconv_status_t igconv_set_tuning(igconv_tune_key_t key, int value) {
     case IGCONV_TUNE_ONE_ISSUER:
       if (value < 0 || value > 1) return IGCONV_ERR_INVALID_ARG;
       g_tune_one_issuer.store(value);
+      return IGCONV_OK;
+    case IGCONV_TUNE_WGRAD_HALO:
+      if (value < 0 || value > 1) return IGCONV_ERR_INVALID_ARG;
+      g_tune_wgrad_halo.store(value);
       return IGCONV_OK;
   }
   return IGCONV_ERR_INVALID_ARG;
@@ -1892,6 +1985,8 @@ size_t conv2d_wgrad_workspace_size(const igconv_problem_t* prob, igconv_dtype_t 
     return round256(static_cast<size_t>(prob->N) * prob->H * prob->W * 16) + w.ws_bytes;
   }
   plan_wgrad_shape(prob, P, Q, sm_count, &w);
+  WgradHaloPlan hp;
+  if (plan_wgrad_halo(prob, P, Q, sm_count, &hp) && hp.ws_bytes > w.ws_bytes) return hp.ws_bytes;
   return w.ws_bytes;
 }
 
@@ -1941,6 +2036,11 @@ igconv_status_t conv2d_wgrad(const igconv_problem_t* prob, igconv_dtype_t dtype,
     return IGCONV_ERR_MISALIGNED;
   DeviceState* dev = nullptr;
   if ((st = device_state(&dev)) != IGCONV_OK) return st;
+  WgradHaloPlan hp;
+  if (plan_wgrad_halo(prob, P, Q, dev->sm_count, &hp) && workspace &&
+      workspace_bytes >= hp.ws_bytes)  // (a smaller workspace takes the plan below)
+    return run_wgrad_halo(prob, P, Q, hp, bf16, X, dY, workspace, dev, dW, dw_dtype, Cin, alpha,
+                          beta, s);
   WgradPlan w;
   plan_wgrad_shape(prob, P, Q, dev->sm_count, &w);
   if (!workspace || workspace_bytes < w.ws_bytes) return IGCONV_ERR_WORKSPACE;

@@ -167,6 +167,9 @@ cudaError_t launch_conv_gemm(const ConvGemmParams& p, int block_n, int grid, cud
 cudaError_t launch_conv_gemm_s16(const ConvGemmParams& p, int block_n, int grid, cudaStream_t s);
 // The halo kernel (a plan with p.halo set: 64-wide tiles, 16-bit stores).
 cudaError_t launch_conv_gemm_halo(const ConvGemmParams& p, int grid, cudaStream_t s);
+// The wgrad halo kernel (conv_wgrad_halo.cu): p.splits CTAs, each one unit of
+// p.kblocks_total 128-position blocks; partial tiles to p.out (see there).
+cudaError_t launch_wgrad_halo(const ConvGemmParams& p, cudaStream_t s);
 // Clusters of two CTAs of the kernel with this tile width that fit at once.
 int conv_gemm_pair_capacity(int block_n);
 size_t conv_gemm_smem_bytes(int block_n);

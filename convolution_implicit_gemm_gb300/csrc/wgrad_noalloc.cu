@@ -102,7 +102,9 @@ extern "C" igconv_status_t conv2d_wgrad_noalloc(const igconv_problem_t* prob,
     // an invalid problem: let the regular entry point name the error
     return conv2d_wgrad(prob, dtype, dw_dtype, X, dY, Cin, dW, alpha, beta, nullptr, 0, stream);
   }
-  if (need > static_cast<size_t>(IGCONV_WGRAD_NOALLOC_SCRATCH_BYTES)) return IGCONV_ERR_WORKSPACE;
+  // (a problem whose fastest plan needs more than the scratch array may still
+  // fit its split-K plan; conv2d_wgrad picks the plan the size allows and
+  // returns WORKSPACE when none fits)
   void* scratch = nullptr;
   const igconv_status_t st = scratch_address(&scratch);
   if (st != IGCONV_OK) return st;

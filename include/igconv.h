@@ -219,11 +219,15 @@ IGCONV_API size_t conv2d_wgrad_workspace_size(const igconv_problem_t *prob,
  *   dw_dtype  IGCONV_F16, IGCONV_BF16 or IGCONV_F32 for dW and Cin.
  *   X [N][H][W][C]   dY [N][P][Q][K]   dW [K][R][S][C] (written)
  *   Cin [K][R][S][C], read only when beta != 0.
- *   workspace  device memory of at least conv2d_wgrad_workspace_size() bytes,
- *              owned by the caller; contents need not be initialised and are
- *              overwritten.  It must not be used by another call that runs
- *              concurrently.
- * Errors: as conv2d_fprop; WORKSPACE if workspace is NULL or too small. */
+ *   workspace  device memory of conv2d_wgrad_workspace_size() bytes (what the
+ *              fastest plan for the problem needs), owned by the caller;
+ *              contents need not be initialised and are overwritten.  A
+ *              smaller workspace that still holds the split-K plan's
+ *              partials runs that plan instead of the halo plan (see
+ *              IGCONV_TUNE_WGRAD_HALO).  It must not be used by another call
+ *              that runs concurrently.
+ * Errors: as conv2d_fprop; WORKSPACE if workspace is NULL or smaller than
+ * every plan needs. */
 IGCONV_API igconv_status_t conv2d_wgrad(const igconv_problem_t *prob, igconv_dtype_t dtype,
                                         igconv_dtype_t dw_dtype, const void *X, const void *dY,
                                         const void *Cin, void *dW, float alpha, float beta,
@@ -254,9 +258,9 @@ IGCONV_API igconv_status_t conv2d_wgrad(const igconv_problem_t *prob, igconv_dty
  *   on the GPU (other streams, other host threads) race and must be
  *   serialised by the caller.  Every partial a call reads was written by the
  *   same call, so nothing needs clearing between calls.
- * Errors: as conv2d_wgrad; IGCONV_ERR_WORKSPACE when the problem needs more
- * than IGCONV_WGRAD_NOALLOC_SCRATCH_BYTES of partial sums (compare
- * conv2d_wgrad_workspace_size() with the limit). */
+ * Errors: as conv2d_wgrad; IGCONV_ERR_WORKSPACE when no plan's partial sums
+ * fit IGCONV_WGRAD_NOALLOC_SCRATCH_BYTES (a problem whose size query exceeds
+ * the limit may still run its split-K plan). */
 IGCONV_API igconv_status_t conv2d_wgrad_noalloc(const igconv_problem_t *prob,
                                                 igconv_dtype_t dtype, igconv_dtype_t dw_dtype,
                                                 const void *X, const void *dY, const void *Cin,
@@ -632,6 +636,18 @@ IGCONV_API const char *igconv_status_string(igconv_status_t status);
  *                             accumulators.  The two add the blocks in
  *                             different orders: exact alike on integer data,
  *                             each deterministic otherwise.
+ *   IGCONV_TUNE_WGRAD_HALO    conv2d_wgrad with stride 1, C and K at most 64
+ *                             and 2..9 filter taps: 0 runs on input halos
+ *                             (one copy of a block's input rows for every
+ *                             tap, every tap pair of a split in one CTA;
+ *                             the built-in choice where the output width
+ *                             fits a grid of 32, 64 or 128 columns, P is a
+ *                             multiple of 128 / that width and the
+ *                             workspace holds its partials); 1 never.  The
+ *                             two sum the positions in different orders:
+ *                             exact alike on integer data, each
+ *                             deterministic otherwise.  Query the workspace
+ *                             size after setting it.
  * Returns INVALID_ARG for an unknown key or value. */
 typedef enum {
     IGCONV_TUNE_WGRAD_SPLITS = 1,
@@ -646,7 +662,8 @@ typedef enum {
     IGCONV_TUNE_DGRAD_ROWS = 10,
     IGCONV_TUNE_EPILOGUE_KERNEL = 11,
     IGCONV_TUNE_HALO = 12,
-    IGCONV_TUNE_ONE_ISSUER = 13
+    IGCONV_TUNE_ONE_ISSUER = 13,
+    IGCONV_TUNE_WGRAD_HALO = 14
 } igconv_tune_key_t;
 IGCONV_API igconv_status_t igconv_set_tuning(igconv_tune_key_t key, int value);
 

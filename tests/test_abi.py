@@ -187,6 +187,9 @@ def test_tuning_keys(igc):
     assert lib.igconv_set_tuning(igc.TUNE_ONE_ISSUER, 2) == 1
     assert lib.igconv_set_tuning(igc.TUNE_ONE_ISSUER, 1) == 0
     assert lib.igconv_set_tuning(igc.TUNE_ONE_ISSUER, 0) == 0
+    assert lib.igconv_set_tuning(igc.TUNE_WGRAD_HALO, 2) == 1
+    assert lib.igconv_set_tuning(igc.TUNE_WGRAD_HALO, 1) == 0
+    assert lib.igconv_set_tuning(igc.TUNE_WGRAD_HALO, 0) == 0
 
 
 def test_grouped_reject_invalid(igc):

@@ -102,9 +102,17 @@ def test_fixed_split_is_deterministic():
 
 
 def test_workspace_too_small_is_rejected():
+    """Below the smallest plan's workspace (the split-K plan's partials; the
+    size query reports the halo plan's larger need where that plan applies)
+    the call is refused."""
     pb = WORKLOADS["tiny"]["problem"]
     inp, P, Q = inputs(pb, "f16", "int_uniform", 1)
-    need = igc.conv2d_wgrad_workspace_size(pb, torch.float16, torch.float16)
+    try:
+        igc.igconv_set_tuning(igc.TUNE_WGRAD_HALO, 1)
+        need = igc.conv2d_wgrad_workspace_size(pb, torch.float16, torch.float16)
+    finally:
+        igc.igconv_set_tuning(igc.TUNE_WGRAD_HALO, 0)
+    assert igc.conv2d_wgrad_workspace_size(pb, torch.float16, torch.float16) >= need
     ws = torch.empty(need, dtype=torch.uint8, device="cuda")
     dW = torch.empty(pb["K"], pb["R"], pb["S"], pb["C"], dtype=torch.float16, device="cuda")
     with pytest.raises(igc.IgconvError) as e:
