@@ -64,6 +64,11 @@ cudaError_t launch_conv_gemm(const ConvGemmParams& p_in, int block_n, int grid, 
   ConvGemmParams p = p_in;
   const bool fits = block_n == 64 && !p.pair && p.epi != EPI_PARTIAL && 4 * p.num_acc * 64 <= 512;
   p.epi_groups = (fits && p.epi_groups != 1) ? 2 : 1;
+  // every unit of a conv plan has blocks unless a sub-problem has none (a
+  // residue class no tap reaches)
+  p.all_acc = p.epi != EPI_PARTIAL;
+  for (int i = 0; i < p.nsub; ++i)
+    if (p.sub[i].rcount * p.sub[i].scount * p.cblocks <= 0) p.all_acc = 0;
   // halo and one-issuer plans store 64-column boxes, whole tile rows per
   // warp: two groups always
   if (p.halo || (p.one_issuer && block_n == 64)) p.epi_groups = 2;

@@ -207,6 +207,11 @@ struct UnitWalk {
   bool fast;
 };
 
+// Whether walk_begin takes the fast path for these scalars.
+__device__ __forceinline__ bool uw_fast_possible(const Sched& sc) {
+  return sc.epi != EPI_PARTIAL && sc.raster <= 1;
+}
+
 // Places a fast walk at unit it.u (< units).
 __device__ __forceinline__ void walk_seek(const ConvGemmParams& p, const Sched& sc,
                                           UnitWalk& it) {
@@ -225,7 +230,7 @@ __device__ __forceinline__ void walk_begin(const ConvGemmParams& p, const Sched&
                                            UnitWalk& it) {
   it.u = unit_first(sc);
   it.stride = unit_stride(sc);
-  it.fast = sc.epi != EPI_PARTIAL && sc.raster <= 1;
+  it.fast = uw_fast_possible(sc);
   it.tm = it.tn = it.gq = it.gr = it.nk = it.sub = 0;
   it.sub_end = sc.units;
   it.mstep = sc.pair ? 2 : 1;
@@ -1128,7 +1133,16 @@ __device__ __forceinline__ void run_epilogue(const ConvGemmParams& p, uint64_t* 
   const int M0 = p.sub[0].M;  // GEMM rows when there is one sub-problem
   const bool one_sub = e.sc.nsub == 1;
   UnitWalk uw;
+  // Every unit has blocks (p.all_acc): tile parity alone names the group, so
+  // the other group's units are passed over before any decoding (on the fast
+  // walk their block count comes with the walk).
+  const bool skip_fast = groups == 2 && p.all_acc && uw_fast_possible(e.sc);
   for (walk_begin(p, e.sc, uw); uw.u < e.sc.units; walk_next(p, e.sc, uw)) {
+    if (skip_fast && (local & 1) != group) {
+      qseq += uw.nk;
+      ++local;
+      continue;
+    }
     const Work w = walk_work(p, e.sc, uw);
     const int nk = w.kb1 - w.kb0;
     const bool has_acc = nk > 0;

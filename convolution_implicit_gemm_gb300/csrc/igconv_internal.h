@@ -93,6 +93,7 @@ struct ConvGemmParams {
                               // the input, box (64 channels, Ws pixels, halo rows, 1); sub[0]
                               // is the stride-1 plan on a grid Ws = 32/64/128 columns wide
   int halo_bytes;             // bytes one halo copy lands (the whole box)
+  int all_acc;                // set by the launcher: every unit has reduction blocks
   int one_issuer;             // halo plans: the two MMA issuers take alternate units whole,
                               // each into the unit's one accumulator (num_acc = 1)
   int store_5d;               // strided dgrad: mapY is dX viewed as (c, w % sw, w / sw, h % sh,
