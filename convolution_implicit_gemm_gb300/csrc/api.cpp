@@ -1421,21 +1421,25 @@ igconv_status_t run_wgrad(const igconv_problem_t* g, int P, int Q, const WgradPl
                                        remap));
 }
 
-// wgrad on input halos (conv_wgrad_halo.cu): stride 1, C and K at most 64,
+// wgrad on input halos (conv_wgrad_halo.cu): stride 1, C and K at most 128,
 // 2..kHaloTaps taps.  Output positions run on a grid Wt = 32, 64 or 128
 // columns wide (the smallest that holds Q + the largest column offset), in
 // blocks of 128 positions = 128 / Wt whole output rows, so P must be a
 // multiple of 128 / Wt; each block's input halo of HR = 128 / Wt + the
-// largest row offset + 1 rows must fit kHaloRows.  One unit (CTA) per split,
-// at most one per SM, each computing every tap pair of its blocks; the
-// partial tiles are [split][pairs * 128][64] fp32.
+// largest row offset + 1 rows per 64-channel plane and its dY rows per
+// 64-channel chunk form one pipeline stage (two or three must fit).  The
+// GEMM rows are (tap, plane) entries of 64 rows, two per 128-row M-tile; a
+// CTA takes one split of the blocks for a group of M-tiles (as many as fit
+// TMEM at N = 64 or 128 columns each, the groups balanced), at most one CTA
+// per SM in all; the partial tiles are [split][tiles * 128][N] fp32.
 struct WgradHaloPlan {
-  int wt, rows, hr, blocks, splits, pairs;
+  int wt, rows, hr, blocks, splits, planes, kchunks, tiles, group_tiles, groups;
+  int stage_bytes, stages;
   size_t ws_bytes;
 };
 bool plan_wgrad_halo(const igconv_problem_t* pb, int P, int Q, int sm_count, WgradHaloPlan* h) {
   if (g_tune_wgrad_halo.load() == 1) return false;
-  if (pb->stride_h != 1 || pb->stride_w != 1 || pb->C > 64 || pb->K > 64) return false;
+  if (pb->stride_h != 1 || pb->stride_w != 1 || pb->C > 128 || pb->K > 128) return false;
   const int taps = pb->R * pb->S;
   if (taps < 2 || taps > kHaloTaps) return false;
   const int max_h = (pb->R - 1) * pb->dil_h, max_w = (pb->S - 1) * pb->dil_w;
@@ -1446,13 +1450,24 @@ bool plan_wgrad_halo(const igconv_problem_t* pb, int P, int Q, int sm_count, Wgr
   h->rows = kBlockM / wt;
   h->hr = h->rows + max_h + 1;
   if (h->hr * wt > kHaloRows || h->hr > 256 || P % h->rows != 0) return false;
+  h->planes = ceil_div(pb->C, 64);
+  h->kchunks = ceil_div(pb->K, 64);
+  h->stage_bytes = h->planes * h->hr * wt * 128 + h->kchunks * kBlockM * 128;
+  // stages, epilogue staging (32 KB), barriers and the base alignment in 227 KB
+  const int room = 232448 - 32768 - 256 - 1024;
+  h->stages = std::min(3, room / h->stage_bytes);
+  if (h->stages < 2) return false;
   const long long blocks = static_cast<long long>(pb->N) * (P / h->rows);
   if (blocks < 1 || blocks > INT_MAX) return false;
   h->blocks = static_cast<int>(blocks);
+  const int N = 64 * h->kchunks;
+  h->tiles = (taps * h->planes + 1) / 2;
+  const int max_tiles = std::min(8, 512 / N);
+  h->groups = ceil_div(h->tiles, max_tiles);
+  h->group_tiles = ceil_div(h->tiles, h->groups);
   const int sms = sm_count > 0 ? sm_count : 148;
-  h->splits = h->blocks < sms ? h->blocks : sms;
-  h->pairs = (taps + 1) / 2;
-  h->ws_bytes = static_cast<size_t>(h->splits) * h->pairs * kBlockM * 64 * sizeof(float);
+  h->splits = std::max(1, std::min(h->blocks, sms / h->groups));
+  h->ws_bytes = static_cast<size_t>(h->splits) * h->tiles * kBlockM * N * sizeof(float);
   return true;
 }
 
@@ -1485,28 +1500,34 @@ igconv_status_t run_wgrad_halo(const igconv_problem_t* g, int P, int Q, const Wg
   sp.lower_w = -g->pad_w;
   sp.r0 = 0; sp.rstep = 1; sp.rcount = g->R; sp.offh0 = 0; sp.doffh = g->dil_h;
   sp.s0 = 0; sp.sstep = 1; sp.scount = g->S; sp.offw0 = 0; sp.doffw = g->dil_w;
+  const int N = 64 * h.kchunks;
   p.nsub = 1;
   p.epi = EPI_PARTIAL;
   p.splits = h.splits;
   p.kblocks_total = h.blocks;
-  p.tiles_m_total = h.pairs;
+  p.tiles_m_total = h.tiles;
+  p.num_acc = h.group_tiles;
+  p.cblocks = h.planes;
+  p.tiles_n = h.kchunks;
   p.halo_bytes = h.hr * h.wt * 128;
-  p.idesc = make_idesc(kBlockM, 64, bf16, 1, 1);
+  p.wh_stage_bytes = h.stage_bytes;
+  p.wh_stages = h.stages;
+  p.idesc = make_idesc(kBlockM, N, bf16, 1, 1);
   p.out = part;
   if (!encode_nhwc_box(&p.mapA[0], X, bf16, g->N, g->H, g->W, g->C, h.wt, h.hr) ||
       !encode_nhwc_box(&p.mapB, dY, bf16, g->N, P, Q, g->K, h.wt, h.rows) ||
       !encode_out_2d(&p.mapY, part, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
-                     static_cast<long long>(h.splits) * h.pairs * kBlockM, 64, 16,
+                     static_cast<long long>(h.splits) * h.tiles * kBlockM, N, 16,
                      CU_TENSOR_MAP_SWIZZLE_64B))
     return IGCONV_ERR_UNSUPPORTED;
   p.mapA_valid = 1u;
   p.use_tma_store = 1;
   if (launch_wgrad_halo(p, s) != cudaSuccess) return IGCONV_ERR_CUDA;
   const int dwt = dw_dtype == IGCONV_F32 ? 2 : (dw_dtype == IGCONV_BF16 ? 1 : 0);
-  const int rows = h.pairs * kBlockM;
+  const int rows = h.tiles * kBlockM;
   return from_cuda(launch_wgrad_reduce(static_cast<const float*>(part), h.splits,
-                                       static_cast<long long>(rows) * 64, 64, rows, 64, 0, g->K,
-                                       g->R * g->S, g->C, 64, dW, dwt,
+                                       static_cast<long long>(rows) * N, N, rows, N, 0, g->K,
+                                       g->R * g->S, g->C, 64 * h.planes, dW, dwt,
                                        beta != 0.0f ? Cin : nullptr, alpha, beta, s, nullptr));
 }
 

@@ -92,7 +92,11 @@ struct ConvGemmParams {
   int halo;                   // 1: halo plan (conv_gemm_halo_kernel): mapA[0] is a tiled map of
                               // the input, box (64 channels, Ws pixels, halo rows, 1); sub[0]
                               // is the stride-1 plan on a grid Ws = 32/64/128 columns wide
-  int halo_bytes;             // bytes one halo copy lands (the whole box)
+  int halo_bytes;             // bytes one halo copy lands (the whole box; wgrad: one channel
+                              // plane of it)
+  int wh_stage_bytes;         // wgrad halo plans: bytes per pipeline stage (the input planes
+                              // and the dY chunks of one block), and the stage count
+  int wh_stages;
   int all_acc;                // set by the launcher: every unit has reduction blocks
   int one_issuer;             // halo plans: the two MMA issuers take alternate units whole,
                               // each into the unit's one accumulator (num_acc = 1)

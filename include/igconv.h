@@ -636,7 +636,7 @@ IGCONV_API const char *igconv_status_string(igconv_status_t status);
  *                             accumulators.  The two add the blocks in
  *                             different orders: exact alike on integer data,
  *                             each deterministic otherwise.
- *   IGCONV_TUNE_WGRAD_HALO    conv2d_wgrad with stride 1, C and K at most 64
+ *   IGCONV_TUNE_WGRAD_HALO    conv2d_wgrad with stride 1, C and K at most 128
  *                             and 2..9 filter taps: 0 runs on input halos
  *                             (one copy of a block's input rows for every
  *                             tap, every tap pair of a split in one CTA;

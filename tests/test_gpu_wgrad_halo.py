@@ -1,11 +1,12 @@
-"""GPU parity of conv2d_wgrad on input halos (stride 1, C and K at most 64,
-2..9 filter taps).
+"""GPU parity of conv2d_wgrad on input halos (stride 1, C and K at most
+128, 2..9 filter taps).
 
 Output positions run on a grid 32, 64 or 128 columns wide in blocks of 128
-positions; each block's input rows (the halo) and dY rows are copied once
-for all taps, taps are paired into 128-row MMA tiles whose two halves point
-at their taps' rows, one CTA computes every tap pair of its split, and the
-ordered split reduction finishes dW.  Compared with the oracle (exact on
+positions; each block's input rows (the halo, per 64-channel plane) and dY
+rows (per 64-channel chunk) are copied once for all taps; (tap, plane)
+entries pair into 128-row MMA tiles whose two halves point at their rows; a
+CTA computes a group of tiles over its split, and the ordered split
+reduction finishes dW.  Compared with the oracle (exact on
 integer-valued data, alpha / beta, fp32 and 16-bit dW), with the split-K
 plan (IGCONV_TUNE_WGRAD_HALO = 1; same values on integer data, both within
 the bound and repeatable on random data), and with a workspace too small for
@@ -69,6 +70,9 @@ SHAPES = [
     problem(1, 16, 24, 40, 64, 3, 3, (2, 2), (1, 1), (2, 2)),   # dilation 2
     problem(2, 20, 40, 16, 24, 1, 5, (0, 2)),                   # 1 x 5 taps
     problem(1, 11, 61, 64, 16, 2, 2, (1, 1)),                   # 2 x 2 taps, 64-wide grid
+    problem(2, 28, 28, 128, 128, 3, 3, (1, 1)),                 # two planes, N = 128, 3 groups
+    problem(1, 16, 24, 96, 80, 3, 3, (2, 2), (1, 1), (2, 2)),   # ragged planes and chunks
+    problem(1, 20, 30, 128, 64, 3, 1, (1, 0)),                  # two planes, N = 64
 ]
 
 
@@ -84,7 +88,7 @@ def test_wgrad_halo_integer_exact(pb):
 
 
 @pytest.mark.parametrize("dw_dtype", ["bf16", "f32"])
-@pytest.mark.parametrize("pb", [SHAPES[0], SHAPES[2]], ids=_id)
+@pytest.mark.parametrize("pb", [SHAPES[0], SHAPES[2], SHAPES[5]], ids=_id)
 def test_wgrad_halo_random_within_bound_and_deterministic(pb, dw_dtype):
     inp, P, Q = inputs(pb, "bf16", "normal_he", 131, dw_dtype=dw_dtype)
     want, A = ref(pb, inp)
