@@ -746,12 +746,14 @@ __device__ __forceinline__ void run_mma(const ConvGemmParams& p, uint8_t* pipe, 
     }
     tc_fence_after_sync();
   }
-  // One issuer per unit (p.one_issuer, 64-wide plans of short reductions):
-  // the issuers take alternate units whole, each into the unit's one
-  // accumulator.  A stage then serves both issuers over time, so the issuer
-  // also waits, in order, for the fills of the units it skips: having seen
-  // every fill of every stage, its parity wait on a stage cannot be passed by
-  // the phase before.
+  // One issuer per unit (p.one_issuer, 64-wide plans of short reductions): the issuers take alternate units whole, each into the
+  // unit's one accumulator.  A stage then serves both issuers over time, so
+  // both take part in every stage's release: the issuer that skips a unit
+  // waits for each of its fills in order and arrives on the stage's empty
+  // barrier (count 2), the other commits there after its MMAs.  The producer
+  // cannot refill a stage before both have seen the fill, so neither issuer
+  // can fall two phases behind on a stage (where a parity wait would take
+  // the phase after next for the one it wants, and never end).
   const bool one = NI == 2 && p.one_issuer != 0;
   const int rstep = one ? 1 : NI;
   UnitWalk uw;
@@ -768,6 +770,8 @@ __device__ __forceinline__ void run_mma(const ConvGemmParams& p, uint8_t* pipe, 
           ok = false;
           break;
         }
+        if (lane == 0) mbar_arrive(&empty[st]);  // this issuer's release of the fill
+        __syncwarp();
         if (++st == STAGES) {
           st = 0;
           ph ^= 1u;
@@ -1618,7 +1622,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], p.one_issuer ? 2 : 1);  // one issuer per unit: both release
     }
     // a tile's epilogue is 8 warps (one group) or 4 (two groups); with pairs
     // the even CTA's TMEM-empty barriers count both CTAs' epilogues
@@ -1730,9 +1734,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 // on the GPU: with the field set to the start's row within the pattern the
 // products were wrong, with it zero exact).  The two issuers take alternate
 // units whole (p.one_issuer), each into the unit's single accumulator, so
-// the epilogue reads one accumulator and stores 64-column boxes; without
-// one_issuer both read every halo (each the blocks of its sequence parity)
-// and a stage is free once both have committed.  Junk columns (grid column >= the output width)
+// the epilogue reads one accumulator and stores 64-column boxes; the other
+// issuer still waits for each halo and arrives on its empty barrier, so a
+// stage is free only once both issuers have seen it (without one_issuer
+// both read every halo, each the blocks of its sequence parity).  Junk columns (grid column >= the output width)
 // read neighbouring pixels; the epilogue drops them (ws_valid, and the
 // output map clips them).
 // ---------------------------------------------------------------------------
@@ -1861,13 +1866,17 @@ __device__ __forceinline__ void run_mma_halo(const ConvGemmParams& p, uint8_t* p
   for (walk_begin(p, sc, uw); ok && uw.u < sc.units; walk_next(p, sc, uw)) {
     if (one && (local & 1) != issuer) {
       // The other issuer's unit.  With three stages consecutive fills of a
-      // stage belong to different issuers, so this issuer still waits for
-      // the fill to land: having seen every fill of a stage in order, its
-      // parity wait on the next one cannot be passed by the phase before.
+      // stage belong to different issuers, so both take part in every
+      // stage's release: this issuer waits for the fill and arrives on the
+      // stage's empty barrier (count 2).  The producer cannot refill the stage
+      // before both have seen the fill, so neither can fall two phases
+      // behind (where its parity wait would take the phase after next).
       if (!__all_sync(0xffffffffu, mbar_wait(&full[st], ph, abort_flag, timeout))) {
         if (lane == 0) report_failure(p, abort_flag, DEVERR_MMA_FULL_WAIT);
         break;
       }
+      if (lane == 0) mbar_arrive(&empty[st]);
+      __syncwarp();
       if (++st == C::STAGES) {
         st = 0;
         ph ^= 1u;
@@ -1970,16 +1979,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_cols = tmem_cols_for(static_cast<uint32_t>(nbuf * p.num_acc * 64));
 
   if (threadIdx.x == 0) {
-    // one issuer per unit (one_issuer): each halo and accumulator has one
-    // consumer / producer; otherwise both issuers read every halo
-    const int consumers = p.one_issuer ? 1 : C::NI;
+    // both issuers release every halo (one_issuer: the unit's issuer by its
+    // commit, the other by an arrive after seeing the fill); each accumulator
+    // has one issuer with one_issuer, else both
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], consumers);
+      mbar_init(&empty[s], C::NI);
     }
     const int epi_warps = p.epi_groups == 2 ? kEpiWarps / 2 : kEpiWarps;
     for (int b = 0; b < 4; ++b) {
-      mbar_init(&tfull[b], consumers);
+      mbar_init(&tfull[b], p.one_issuer ? 1 : C::NI);
       mbar_init(&tempty[b], epi_warps);
     }
     mbar_init(&done_bar[0], 1);

@@ -3,10 +3,12 @@
 fprop and dgrad with 64-wide tiles of at most four reduction blocks (1x1
 layers, the packed stem, strided dgrad's residue classes, small filters)
 give each tile to one of the two MMA issuers, which adds all its blocks into
-one accumulator; the epilogue stores 64-column boxes.  A stage of the ring
+one accumulator; two epilogue groups take alternate tiles and store
+64-column boxes.  A stage of the ring
 then serves both issuers over time (with three blocks per tile, consecutive
 fills of a stage go to different issuers), so the issuer that skips a tile
-still waits for its fills.  IGCONV_TUNE_ONE_ISSUER = 1 keeps two issuers per
+still waits for each of its fills and arrives on the stage's empty barrier:
+a stage is refilled only after both issuers have seen it.  IGCONV_TUNE_ONE_ISSUER = 1 keeps two issuers per
 tile.  Both settings must be exact against the oracle on integer data and
 repeat bit for bit on random data.
 """
@@ -67,6 +69,11 @@ CASES = [
     ("dgrad", problem(2, 23, 21, 64, 64, 3, 3, (1, 1), (2, 2))),   # residue classes 1-4 blocks
     ("dgrad", problem(2, 28, 56, 64, 64, 3, 3, (1, 1), (2, 2))),   # classes on 5D rows
     ("fprop", problem(2, 40, 42, 3, 64, 7, 7, (3, 3), (2, 2))),    # packed stem: 4 blocks
+    # 1x1 fprop with K > 64 (wider tiles, two accumulators or one issuer)
+    ("fprop", problem(2, 15, 13, 64, 256, 1, 1)),                  # 1x1 64 -> 256
+    ("fprop", problem(2, 9, 11, 128, 192, 1, 1)),                  # 2 blocks, K ragged by tile
+    ("fprop", problem(1, 7, 9, 96, 136, 1, 1)),                    # C and K ragged
+    ("fprop", problem(1, 5, 5, 16, 1096, 1, 1)),                   # bias too long to stage
 ]
 
 
