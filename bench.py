@@ -343,31 +343,51 @@ def timed_launches(fn, stream):
 
 
 class GraphStep:
-    """One bench step (fprop, dgrad, wgrad of every layer) captured into a
-    CUDA graph, with timing events around each call and around the step."""
+    """One bench step (fprop, dgrad, wgrad of every layer) captured into CUDA
+    graphs.  An event-record node between two kernels of a graph costs about
+    7 us per call here (the step measured 0.632 ms with an event pair around
+    each of its 15 calls and 0.526 ms without), so the timed step `g` holds
+    the calls alone between the two step events.  `g_pass[kind]` holds the
+    five calls of one pass kind alone (per-pass rates and the implicit-GEMM
+    launch time), and `g_calls` the step with an event pair around each call
+    (the per-layer table, which therefore includes those nodes)."""
 
     def __init__(self, layers):
         def ev():
             return torch.cuda.Event(enable_timing=True, external=True)
         self.calls = [(kind, L) for L in layers for kind in ("fprop", "dgrad", "wgrad")]
-        self.ev = [(ev(), ev()) for _ in self.calls]
-        self.s0, self.s1 = ev(), ev()
-        self.g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(self.g):
-            self.s0.record()
-            for (kind, L), (a, b) in zip(self.calls, self.ev):
-                a.record()
-                getattr(L, kind)()
-                b.record()
-            self.s1.record()
-        self.g.replay()                    # one untimed replay checks the graph runs
-        torch.cuda.synchronize()
+
+        def capture(calls, per_call):
+            g = torch.cuda.CUDAGraph()
+            s0, s1 = ev(), ev()
+            evs = [(ev(), ev()) for _ in calls] if per_call else None
+            with torch.cuda.graph(g):
+                s0.record()
+                for i, (kind, L) in enumerate(calls):
+                    if per_call:
+                        evs[i][0].record()
+                    getattr(L, kind)()
+                    if per_call:
+                        evs[i][1].record()
+                s1.record()
+            g.replay()                     # one untimed replay checks the graph runs
+            torch.cuda.synchronize()
+            return g, (s0, s1), evs
+
+        self.g, self.ev_step, _ = capture(self.calls, False)
+        self.g_calls, self.ev_calls_step, self.ev_calls = capture(self.calls, True)
+        self.g_pass = {k: capture([(k, L) for L in layers], False)[:2]
+                       for k in ("fprop", "dgrad", "wgrad")}
 
     def step_ms(self):
-        return self.s0.elapsed_time(self.s1)
+        return self.ev_step[0].elapsed_time(self.ev_step[1])
+
+    def pass_ms(self, kind):
+        a, b = self.g_pass[kind][1]
+        return a.elapsed_time(b)
 
     def call_ms(self):
-        return [(kind, L, a.elapsed_time(b)) for (kind, L), (a, b) in zip(self.calls, self.ev)]
+        return [(kind, L, a.elapsed_time(b)) for (kind, L), (a, b) in zip(self.calls, self.ev_calls)]
 
 
 def volume_pass(name, kind, device="cuda"):
@@ -572,6 +592,7 @@ def run_ours(args, rank, world, local_rank):
     clocks.start()
     time.sleep(0.3)
     step_ms, records = [], []
+    pass_graph_ms = {"fprop": [], "dgrad": [], "wgrad": []}
     torch.cuda.synchronize()
     for _ in range(args.steps):
         flush.zero_()                      # L2 flushed between timed steps, outside the timing
@@ -579,7 +600,6 @@ def run_ours(args, rank, world, local_rank):
             graph.g.replay()
             torch.cuda.synchronize()
             step_ms.append(graph.step_ms())
-            records.append(graph.call_ms())
         else:
             rec = []
             a, b = timed_launches(lambda: step(rec), stream)
@@ -589,6 +609,19 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     clk = clocks.stop()
     status = {"timed_steps": require_device_ok(igc, "the timed steps")}
+    if graph is not None:
+        # the per-pass graphs and the per-call graph, each from a flushed L2
+        for _ in range(min(args.steps, 50)):
+            for kind in pass_graph_ms:
+                flush.zero_()
+                graph.g_pass[kind][0].replay()
+                torch.cuda.synchronize()
+                pass_graph_ms[kind].append(graph.pass_ms(kind))
+            flush.zero_()
+            graph.g_calls.replay()
+            torch.cuda.synchronize()
+            records.append(graph.call_ms())
+        status["pass_graphs"] = require_device_ok(igc, "the per-pass graphs")
     check = None
     if rank == 0 and not args.no_check:
         check = check_outputs(layers, args.check_samples, 777)
@@ -602,6 +635,8 @@ def run_ours(args, rank, world, local_rank):
             graph.g.replay()
             torch.cuda.synchronize()
             warm_ms.append(graph.step_ms())
+            graph.g_calls.replay()
+            torch.cuda.synchronize()
             warm_records.append(graph.call_ms())
         else:
             rec = []
@@ -623,11 +658,20 @@ def run_ours(args, rank, world, local_rank):
             pass_ms[kind] += ms
             pass_flops[kind] += L.flops
             per_layer.setdefault(L.name, {}).setdefault(kind, 0.0)
-            per_layer[L.name][kind] += ms / args.steps
+            per_layer[L.name][kind] += ms / len(records)
             if kind in ("fprop", "dgrad"):
                 gemm_ms += ms
                 gemm_flops += L.flops
                 gemm_launches += 1
+    gemm_launches //= max(1, len(records))
+    if graph is not None:
+        # per-pass rates and the implicit-GEMM launch time from the graphs of
+        # one pass kind each (no event nodes between their kernels)
+        for kind, v in pass_graph_ms.items():
+            pass_ms[kind] = sum(v)
+            pass_flops[kind] = len(v) * sum(L.flops for L in layers)
+        gemm_ms = pass_ms["fprop"] + pass_ms["dgrad"]
+        gemm_flops = pass_flops["fprop"] + pass_flops["dgrad"]
     launches_per_step = 4 * len(layers)    # fprop 1, dgrad 1, wgrad 2 (GEMM + reduction)
 
     # end-to-end through the C ABI with host buffers
@@ -688,7 +732,10 @@ def run_ours(args, rank, world, local_rank):
                                       "TFLOP/s": next(L.flops for L in layers if L.name == n)
                                       / (v * 1e-3) / 1e12}
                                   for k, v in d.items()} for n, d in warm_layers.items()}}
-    launch = ("CUDA graph of the step's 15 calls (20 kernels), replayed once per step"
+    launch = ("CUDA graph of the step's 15 calls (20 kernels) between two events, replayed "
+              "once per step; passes and the roofline from graphs of one pass kind each, the "
+              "per-layer table from a graph with an event pair around every call (those "
+              "event nodes add a few us per call)"
               if graph is not None else "stream launches")
     return dict(layers=layers, value=value, ms_per_step=ms_per_step, clocks=clk, e2e=e2e,
                 status=status, check=check, l2_warm=l2_warm,
@@ -1035,7 +1082,7 @@ def workload_config(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--batch", type=int, default=None,
@@ -1099,7 +1146,7 @@ def main():
                                 f"was {sm_mhz} MHz against a maximum of {sm_max} MHz"),
                 "peak_burst": burst, "frac_burst": achieved / burst,
                 "peak_sustained": sustained, "frac_sustained": achieved / sustained,
-                "launches_per_step": gemm_launches // max(1, args.steps),
+                "launches_per_step": gemm_launches,
                 "kernel_source": src_hash}
     line = {"metric": METRIC, "value": res["value"], "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"],

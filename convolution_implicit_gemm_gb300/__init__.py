@@ -37,7 +37,9 @@ __all__ = [
     "fprop", "dgrad", "wgrad", "fprop_int8",
     "F16", "BF16", "F32", "I8", "I32",
     "TUNE_WGRAD_SPLITS", "TUNE_BLOCK_N", "TUNE_MAX_CTAS", "TUNE_CTA_PAIRS", "TUNE_EPI_GROUPS",
-    "TUNE_CONV_SPLITS",
+    "TUNE_CONV_SPLITS", "TUNE_FEW_CHANNELS", "TUNE_RASTER", "TUNE_RESIDENT_FILTER",
+    "TUNE_DGRAD_ROWS", "TUNE_EPILOGUE_KERNEL", "TUNE_HALO", "TUNE_ONE_ISSUER", "TUNE_WGRAD_HALO",
+    "TUNE_PDL",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -47,7 +49,7 @@ F16, BF16, F32, I8, I32 = 0, 1, 2, 3, 4
 TUNE_WGRAD_SPLITS, TUNE_BLOCK_N, TUNE_MAX_CTAS, TUNE_CTA_PAIRS, TUNE_EPI_GROUPS = 1, 2, 3, 4, 5
 TUNE_CONV_SPLITS, TUNE_FEW_CHANNELS, TUNE_RASTER, TUNE_RESIDENT_FILTER = 6, 7, 8, 9
 TUNE_DGRAD_ROWS, TUNE_EPILOGUE_KERNEL, TUNE_HALO, TUNE_ONE_ISSUER = 10, 11, 12, 13
-TUNE_WGRAD_HALO = 14
+TUNE_WGRAD_HALO, TUNE_PDL = 14, 15
 STATUS_NAMES = {0: "IGCONV_OK", 1: "IGCONV_ERR_INVALID_ARG", 2: "IGCONV_ERR_UNSUPPORTED",
                 3: "IGCONV_ERR_MISALIGNED", 4: "IGCONV_ERR_WORKSPACE", 5: "IGCONV_ERR_CUDA",
                 6: "IGCONV_ERR_DEVICE_TIMEOUT"}

@@ -49,7 +49,7 @@ PFN_encodeIm2col g_encode_im2col = nullptr;
 std::atomic<int> g_tune_splits{0}, g_tune_bn{0}, g_tune_max_ctas{0}, g_tune_no_pairs{0},
     g_tune_epi_groups{0}, g_tune_conv_splits{0}, g_tune_few_channels{0}, g_tune_raster{0},
     g_tune_resident_b{0}, g_tune_dgrad_rows{0}, g_tune_general_epi{0}, g_tune_halo{0},
-    g_tune_one_issuer{0}, g_tune_wgrad_halo{0};
+    g_tune_one_issuer{0}, g_tune_wgrad_halo{0}, g_tune_pdl{0};
 
 igconv_status_t device_state(DeviceState** out) {
   int dev = 0;
@@ -1143,6 +1143,10 @@ size_t dw_wgrad_ws_bytes(const DwParams& p) {
 
 }  // namespace
 
+namespace igc {
+bool pdl_enabled() { return g_tune_pdl.load(std::memory_order_relaxed) == 1; }
+}  // namespace igc
+
 // ===========================================================================
 // C ABI
 // ===========================================================================
@@ -1610,6 +1614,10 @@ igconv_status_t igconv_set_tuning(igconv_tune_key_t key, int value) {
     case IGCONV_TUNE_WGRAD_HALO:
       if (value < 0 || value > 1) return IGCONV_ERR_INVALID_ARG;
       g_tune_wgrad_halo.store(value);
+      return IGCONV_OK;
+    case IGCONV_TUNE_PDL:
+      if (value < 0 || value > 1) return IGCONV_ERR_INVALID_ARG;
+      g_tune_pdl.store(value);
       return IGCONV_OK;
   }
   return IGCONV_ERR_INVALID_ARG;

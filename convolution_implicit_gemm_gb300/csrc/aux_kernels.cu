@@ -294,6 +294,8 @@ __global__ void __launch_bounds__(256) wgrad_reduce_many_kernel(
   constexpr int G = 8;      // split groups, one per warp
   constexpr int TR = RPW;   // workspace rows per tile
   __shared__ float part[G][TR][65];
+  pdl_trigger();
+  pdl_wait();  // the partials come from the kernel before this one
   const int g = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int tiles_c = (cols + 63) / 64;
@@ -386,6 +388,8 @@ __global__ void __launch_bounds__(256) wgrad_reduce_kernel(
   constexpr int RPW = 8;      // rows per warp
   constexpr int TR = RPW * RW;  // workspace rows per tile
   __shared__ float part[G][TR][129];
+  pdl_trigger();
+  pdl_wait();  // the partials come from the kernel before this one
   const int t = threadIdx.x;
   const int warp = t >> 5;
   const int lane = t & 31;
@@ -539,18 +543,16 @@ cudaError_t launch_wgrad_reduce(const float* ws, int splits, long long split_str
     while (rpw > 1 && ((rows + rpw - 1) / rpw) * tiles_c < 2LL * sms) rpw >>= 1;
     const long long tiles = ((rows + rpw - 1) / rpw) * tiles_c;
     const unsigned grid = static_cast<unsigned>(tiles < 16384 ? (tiles > 0 ? tiles : 1) : 16384);
-#define IGC_REDUCE_MANY(R)                                                                       \
-  wgrad_reduce_many_kernel<R><<<grid, 256, 0, s>>>(ws, splits, split_stride, ws_ld, rows, cols,  \
-                                                   swapped, K, RS, C, cpad, dW, dw_dtype, cin,  \
-                                                   alpha, beta, remap)
+#define IGC_REDUCE_MANY(R)                                                                     \
+  launch_hot(wgrad_reduce_many_kernel<R>, grid, 256, 0, s, 1, ws, splits, split_stride, ws_ld, \
+             rows, cols, swapped, K, RS, C, cpad, dW, dw_dtype, cin, alpha, beta, remap)
     switch (rpw) {
-      case 8: IGC_REDUCE_MANY(8); break;
-      case 4: IGC_REDUCE_MANY(4); break;
-      case 2: IGC_REDUCE_MANY(2); break;
-      default: IGC_REDUCE_MANY(1); break;
+      case 8: return IGC_REDUCE_MANY(8);
+      case 4: return IGC_REDUCE_MANY(4);
+      case 2: return IGC_REDUCE_MANY(2);
+      default: return IGC_REDUCE_MANY(1);
     }
 #undef IGC_REDUCE_MANY
-    return cudaGetLastError();
   }
   // every split group gets at least two splits, so two loads per row are in flight
   const int G = splits >= 8 ? 4 : (splits >= 4 ? 2 : 1);
@@ -558,23 +560,18 @@ cudaError_t launch_wgrad_reduce(const float* ws, int splits, long long split_str
   const long long tiles = static_cast<long long>((rows + TR - 1) / TR) * ((cols + 127) / 128);
   const unsigned grid = static_cast<unsigned>(tiles < 16384 ? (tiles > 0 ? tiles : 1) : 16384);
 #define IGC_REDUCE(GG)                                                                          \
-  do {                                                                                          \
-    if (swapped)                                                                                \
-      wgrad_reduce_kernel<GG, true><<<grid, 256, 0, s>>>(ws, splits, split_stride, ws_ld, rows, \
-                                                         cols, K, RS, C, cpad, dW, dw_dtype,    \
-                                                         cin, alpha, beta, remap);              \
-    else                                                                                        \
-      wgrad_reduce_kernel<GG, false><<<grid, 256, 0, s>>>(ws, splits, split_stride, ws_ld,      \
-                                                          rows, cols, K, RS, C, cpad, dW,       \
-                                                          dw_dtype, cin, alpha, beta, remap);   \
-  } while (0)
+  (swapped ? launch_hot(wgrad_reduce_kernel<GG, true>, grid, 256, 0, s, 1, ws, splits,          \
+                        split_stride, ws_ld, rows, cols, K, RS, C, cpad, dW, dw_dtype, cin,     \
+                        alpha, beta, remap)                                                     \
+           : launch_hot(wgrad_reduce_kernel<GG, false>, grid, 256, 0, s, 1, ws, splits,         \
+                        split_stride, ws_ld, rows, cols, K, RS, C, cpad, dW, dw_dtype, cin,     \
+                        alpha, beta, remap))
   switch (G) {
-    case 4: IGC_REDUCE(4); break;
-    case 2: IGC_REDUCE(2); break;
-    default: IGC_REDUCE(1); break;
+    case 4: return IGC_REDUCE(4);
+    case 2: return IGC_REDUCE(2);
+    default: return IGC_REDUCE(1);
   }
 #undef IGC_REDUCE
-  return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------

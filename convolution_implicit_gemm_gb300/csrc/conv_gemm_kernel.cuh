@@ -1592,12 +1592,14 @@ template <int BN, bool PAIR, bool VOL, bool RESB = false, bool S16 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     conv_gemm_kernel(const __grid_constant__ ConvGemmParams p) {
   using C = Cfg<BN, PAIR, RESB>;
+  pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   if (static_cast<int>(smem - smem_raw) + C::USED > C::SMEM) {
     // the dynamic shared memory base leaves too little room after aligning
     // it (never seen: the base is 1024-byte aligned); nothing has started yet
+    pdl_wait();
     if (threadIdx.x == 0) atomicCAS(p.status, 0u, static_cast<unsigned int>(DEVERR_SMEM_LAYOUT));
     return;
   }
@@ -1637,6 +1639,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_barrier_init();
   }
+  // the barriers above are this CTA's own: the stream's earlier kernel may
+  // still run until here, not past it (the bias, the inputs, the outputs)
+  pdl_wait();
   if (p.bias_cached) {
     for (int i = threadIdx.x; i < p.N_gemm; i += blockDim.x) {
       if (!S16 && p.epi == EPI_INT8) {
@@ -1954,10 +1959,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     conv_gemm_halo_kernel(const __grid_constant__ ConvGemmParams p) {
   static_assert(BN == 64, "halo plans use 64-wide tiles");
   using C = HaloCfg;
+  pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   if (static_cast<int>(smem - smem_raw) + C::USED > C::SMEM) {
+    pdl_wait();
     if (threadIdx.x == 0) atomicCAS(p.status, 0u, static_cast<unsigned int>(DEVERR_SMEM_LAYOUT));
     return;
   }
@@ -1997,6 +2004,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_barrier_init();
   }
+  // the barriers above are this CTA's own: the stream's earlier kernel may
+  // still run until here, not past it (the bias, the inputs, the outputs)
+  pdl_wait();
   if (p.bias_cached) {
     for (int i = threadIdx.x; i < p.N_gemm; i += blockDim.x) {
       const uint16_t b = static_cast<const uint16_t*>(p.bias)[i];
@@ -2066,8 +2076,8 @@ static cudaError_t launch_bn(const ConvGemmParams& p, int grid, cudaStream_t s) 
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    k<<<grid, kThreads, smem, s>>>(p);
-    return cudaGetLastError();
+    return launch_hot(k, static_cast<unsigned>(grid), kThreads, static_cast<size_t>(smem), s, 1,
+                      p);
   }
   auto* k = conv_gemm_kernel<BN, true, false, false, S16>;
   cudaError_t e = check_launch_regs(reinterpret_cast<const void*>(k));
@@ -2075,19 +2085,7 @@ static cudaError_t launch_bn(const ConvGemmParams& p, int grid, cudaStream_t s) 
   e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   if (grid < 2 || (grid & 1)) return cudaErrorInvalidValue;
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.gridDim = dim3(static_cast<unsigned>(grid));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
-  cfg.stream = s;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k, p);
+  return launch_hot(k, static_cast<unsigned>(grid), kThreads, static_cast<size_t>(smem), s, 2, p);
 }
 
 // Launches a plan on the kernel of tile width block_n (64, 128 or 256),

@@ -16,8 +16,8 @@ cudaError_t launch_conv_gemm_halo(const ConvGemmParams& p, int grid, cudaStream_
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, HaloCfg::SMEM);
   if (e != cudaSuccess) return e;
-  k<<<grid, kThreads, HaloCfg::SMEM, s>>>(p);
-  return cudaGetLastError();
+  return launch_hot(k, static_cast<unsigned>(grid), kThreads, static_cast<size_t>(HaloCfg::SMEM),
+                    s, 1, p);
 }
 
 }  // namespace igc

@@ -240,12 +240,14 @@ __device__ void whalo_epilogue(const ConvGemmParams& p, uint64_t* tfull, uint32_
 __global__ void __launch_bounds__(kThreads, 1)
     conv_wgrad_halo_kernel(const __grid_constant__ ConvGemmParams p) {
   using C = WHaloCfg;
+  pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const int pipe_bytes = p.wh_stages * p.wh_stage_bytes;
   if (static_cast<int>(smem - smem_raw) + pipe_bytes + C::EPI_STAGE + C::BAR_BYTES > C::SMEM ||
       p.wh_stages > C::MAX_STAGES) {
+    pdl_wait();
     if (threadIdx.x == 0) atomicCAS(p.status, 0u, static_cast<unsigned int>(DEVERR_SMEM_LAYOUT));
     return;
   }
@@ -275,6 +277,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  // nothing above touches global memory: the stream's earlier kernel may
+  // still run until here
+  pdl_wait();
 
   if (warp < 4) {
     setmaxnreg_dec<kRegsLow>();
@@ -314,8 +319,8 @@ cudaError_t launch_wgrad_halo(const ConvGemmParams& p, cudaStream_t s) {
   e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, WHaloCfg::SMEM);
   if (e != cudaSuccess) return e;
   const int groups = (p.tiles_m_total + p.num_acc - 1) / p.num_acc;
-  k<<<p.splits * groups, kThreads, WHaloCfg::SMEM, s>>>(p);
-  return cudaGetLastError();
+  return launch_hot(k, static_cast<unsigned>(p.splits * groups), kThreads,
+                    static_cast<size_t>(WHaloCfg::SMEM), s, 1, p);
 }
 
 }  // namespace igc

@@ -242,6 +242,45 @@ __device__ __forceinline__ int requant_rne(long long t, uint32_t mant, int sh,
 }
 #endif
 
+// Whether the implicit-GEMM kernels and the split reductions launch with
+// programmatic dependent launch (tuning knob IGCONV_TUNE_PDL = 1; off by
+// default).  Defined in api.cpp.
+bool pdl_enabled();
+
+#ifdef __CUDACC__
+// Launches kernel k on stream s in clusters of cluster_x CTAs (1: none).
+// With programmatic dependent launch enabled, k may begin launching while
+// the kernel before it in the stream finishes; every kernel launched here
+// calls pdl_wait() before its first global memory access, so the stream's
+// order of memory effects is kept.
+template <typename... Params, typename... Args>
+cudaError_t launch_hot(void (*k)(Params...), unsigned grid, unsigned block, size_t smem,
+                       cudaStream_t s, unsigned cluster_x, Args&&... args) {
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (pdl_enabled()) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, k, static_cast<Args&&>(args)...);
+}
+#endif
+
 // Auxiliary kernels (aux_kernels.cu).
 cudaError_t launch_batched_transpose(const void* src, void* dst, long long batch, long long rows,
                                      long long cols, int elem_bytes, cudaStream_t s);

@@ -415,4 +415,18 @@ __device__ __forceinline__ void tma_load_im2col_4d_pair(void* dst, const CUtenso
       : "memory");
 }
 
+// Programmatic dependent launch.  A kernel launched with the programmatic
+// stream-serialization attribute may start while the kernel before it in the
+// stream still runs.  pdl_wait() blocks until that kernel has completed and
+// its memory writes are visible (for a plain launch it returns at once), so
+// every thread calls it before its first global memory access.
+// pdl_trigger() lets the next such kernel start launching once every CTA of
+// this grid has executed it; since those CTAs are then all resident, the
+// waiting dependents can never keep one of them from running.
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 }  // namespace igc

@@ -648,6 +648,16 @@ IGCONV_API const char *igconv_status_string(igconv_status_t status);
  *                             exact alike on integer data, each
  *                             deterministic otherwise.  Query the workspace
  *                             size after setting it.
+ *   IGCONV_TUNE_PDL           0: plain launches (the built-in choice); 1:
+ *                             the implicit-GEMM kernels and the wgrad split
+ *                             reductions launch with programmatic dependent
+ *                             launch: such a kernel may start while the
+ *                             kernel before it in the stream finishes, and
+ *                             waits for it to complete before it touches
+ *                             global memory, so the stream's order holds.
+ *                             The results are the same either way; in a
+ *                             replayed CUDA graph of back-to-back layers the
+ *                             plain launches measured slightly faster.
  * Returns INVALID_ARG for an unknown key or value. */
 typedef enum {
     IGCONV_TUNE_WGRAD_SPLITS = 1,
@@ -663,7 +673,8 @@ typedef enum {
     IGCONV_TUNE_EPILOGUE_KERNEL = 11,
     IGCONV_TUNE_HALO = 12,
     IGCONV_TUNE_ONE_ISSUER = 13,
-    IGCONV_TUNE_WGRAD_HALO = 14
+    IGCONV_TUNE_WGRAD_HALO = 14,
+    IGCONV_TUNE_PDL = 15
 } igconv_tune_key_t;
 IGCONV_API igconv_status_t igconv_set_tuning(igconv_tune_key_t key, int value);
 

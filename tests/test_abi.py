@@ -190,6 +190,10 @@ def test_tuning_keys(igc):
     assert lib.igconv_set_tuning(igc.TUNE_WGRAD_HALO, 2) == 1
     assert lib.igconv_set_tuning(igc.TUNE_WGRAD_HALO, 1) == 0
     assert lib.igconv_set_tuning(igc.TUNE_WGRAD_HALO, 0) == 0
+    assert lib.igconv_set_tuning(igc.TUNE_PDL, 2) == 1
+    assert lib.igconv_set_tuning(igc.TUNE_PDL, -1) == 1
+    assert lib.igconv_set_tuning(igc.TUNE_PDL, 1) == 0
+    assert lib.igconv_set_tuning(igc.TUNE_PDL, 0) == 0
 
 
 def test_grouped_reject_invalid(igc):
