@@ -13,8 +13,8 @@ Written out, with v*, u* the exact transforms and S[xi] = sum_c |v*||u*|,
 
 which the tests compute in float64 from the inputs (not from the library).
 On small integers in fp16 every step is exact, so the output equals the
-oracle's bit for bit.  The benchmark spec's acceptance bound (max |err| <=
-1e-2 * max sum |x*w|) is checked as well.
+oracle's bit for bit.  The path's acceptance bound for random data (max
+|err| <= 1e-2 * max sum |x*w|) is checked as well.
 """
 import numpy as np
 import pytest
@@ -132,7 +132,7 @@ def test_winograd_random_within_rounding_bound(pb, fmt):
     outs = np.stack(np.unravel_index(np.arange(ref.size), ref.shape), 1)
     W = magnitude_bound(pb, X, Wt, outs).reshape(ref.shape)
     check_bound(got, ref, W, fmt, pb["C"], 0.75, f"winograd {fmt}")
-    # the benchmark spec's acceptance bound on the same outputs
+    # the acceptance bound for random data on the same outputs
     assert float(np.abs(got - ref).max()) <= 1e-2 * float(A.max())
 
 
