@@ -51,9 +51,20 @@ std::atomic<int> g_tune_splits{0}, g_tune_bn{0}, g_tune_max_ctas{0}, g_tune_no_p
     g_tune_resident_b{0}, g_tune_dgrad_rows{0}, g_tune_general_epi{0}, g_tune_halo{0},
     g_tune_one_issuer{0}, g_tune_wgrad_halo{0}, g_tune_pdl{0};
 
+// A failed runtime call (a launch, an attribute, a copy) is reported as
+// IGCONV_ERR_CUDA, and the runtime's last-error state it set is consumed
+// here, so that a later call does not find it and report a second failure
+// (a sticky error stays: the runtime keeps those).
+igconv_status_t cuda_error() {
+  (void)cudaGetLastError();
+  return IGCONV_ERR_CUDA;
+}
+
+igconv_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? IGCONV_OK : cuda_error(); }
+
 igconv_status_t device_state(DeviceState** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return IGCONV_ERR_CUDA;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return cuda_error();
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceState& st = g_dev[dev];
   if (!st.ready) {
@@ -61,9 +72,9 @@ igconv_status_t device_state(DeviceState** out) {
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return IGCONV_ERR_CUDA;
+      return cuda_error();
     st.supported = (major == 10 && minor == 3);  // kernels are built for sm_103a only
-    if (status_word_address(&st.status) != cudaSuccess) return IGCONV_ERR_CUDA;
+    if (status_word_address(&st.status) != cudaSuccess) return cuda_error();
     if (!g_encode_tiled || !g_encode_im2col) {
       cudaDriverEntryPointQueryResult q1, q2;
       void* f1 = nullptr;
@@ -74,7 +85,7 @@ igconv_status_t device_state(DeviceState** out) {
           cudaGetDriverEntryPointByVersion("cuTensorMapEncodeIm2col", &f2, 12000,
                                            cudaEnableDefault, &q2) != cudaSuccess ||
           q2 != cudaDriverEntryPointSuccess)
-        return IGCONV_ERR_CUDA;
+        return cuda_error();
       g_encode_tiled = reinterpret_cast<PFN_encodeTiled>(f1);
       g_encode_im2col = reinterpret_cast<PFN_encodeIm2col>(f2);
     }
@@ -85,7 +96,6 @@ igconv_status_t device_state(DeviceState** out) {
   return IGCONV_OK;
 }
 
-igconv_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? IGCONV_OK : IGCONV_ERR_CUDA; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -1124,7 +1134,7 @@ igconv_status_t plan_dw_wgrad(DwParams& p, const DeviceState* dev, const igconv_
   p.org_w = -pb->pad_w;
   p.tiles = static_cast<long long>(p.tiles_p) * p.tiles_q;
   int occ = 0;
-  if (dw_occupancy(p, &occ) != cudaSuccess) return IGCONV_ERR_CUDA;
+  if (dw_occupancy(p, &occ) != cudaSuccess) return cuda_error();
   if (occ < 1) occ = 1;
   // grouped: one CTA per (chunk, filter tap, split)
   const long long per_split = static_cast<long long>(p.chunks) * (cg > 1 ? pb->R * pb->S : 1);
@@ -1328,8 +1338,8 @@ igconv_status_t wgrad_few_channels(const igconv_problem_t* prob, int P, int Q,
   const long long npq = static_cast<long long>(prob->N) * P * Q;
   if (!encode_2d(&p.mapB, dY, bf16, npq, prob->K)) return IGCONV_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (launch_pad_pixels8(X, X8, pixels, prob->C, s) != cudaSuccess) return IGCONV_ERR_CUDA;
-  if (launch_conv_gemm(p, w.bn, grid_for(p.units, dev), s) != cudaSuccess) return IGCONV_ERR_CUDA;
+  if (launch_pad_pixels8(X, X8, pixels, prob->C, s) != cudaSuccess) return cuda_error();
+  if (launch_conv_gemm(p, w.bn, grid_for(p.units, dev), s) != cudaSuccess) return cuda_error();
   const int dwt = dw_dtype == IGCONV_F32 ? 2 : (dw_dtype == IGCONV_BF16 ? 1 : 0);
   return from_cuda(launch_wgrad_reduce(static_cast<const float*>(part), w.splits,
                                        p.ws_split_stride, w.N_pad,
@@ -1415,7 +1425,7 @@ igconv_status_t run_wgrad(const igconv_problem_t* g, int P, int Q, const WgradPl
   p.mapA_valid = 1u;
   const long long npq = static_cast<long long>(g->N) * P * Q;
   if (!encode_2d(&p.mapB, dY, bf16, npq, g->K)) return IGCONV_ERR_UNSUPPORTED;
-  if (launch_conv_gemm(p, w.bn, grid_for(p.units, dev), s) != cudaSuccess) return IGCONV_ERR_CUDA;
+  if (launch_conv_gemm(p, w.bn, grid_for(p.units, dev), s) != cudaSuccess) return cuda_error();
   const int dwt = dw_dtype == IGCONV_F32 ? 2 : (dw_dtype == IGCONV_BF16 ? 1 : 0);
   const int xext = w.rs * w.cpad;
   return from_cuda(launch_wgrad_reduce(static_cast<const float*>(part), w.splits,
@@ -1526,7 +1536,7 @@ igconv_status_t run_wgrad_halo(const igconv_problem_t* g, int P, int Q, const Wg
     return IGCONV_ERR_UNSUPPORTED;
   p.mapA_valid = 1u;
   p.use_tma_store = 1;
-  if (launch_wgrad_halo(p, s) != cudaSuccess) return IGCONV_ERR_CUDA;
+  if (launch_wgrad_halo(p, s) != cudaSuccess) return cuda_error();
   const int dwt = dw_dtype == IGCONV_F32 ? 2 : (dw_dtype == IGCONV_BF16 ? 1 : 0);
   const int rows = h.tiles * kBlockM;
   return from_cuda(launch_wgrad_reduce(static_cast<const float*>(part), h.splits,
@@ -1703,7 +1713,7 @@ igconv_status_t conv2d_fprop_ws(const igconv_problem_t* prob, igconv_dtype_t dty
     void* Wpk = ws + pw.z_bytes;
     if (launch_few_pack_x(X, Zp, fpk, prob->N, prob->H, prob->W, cs) != cudaSuccess ||
         launch_few_pack_filter(Wt, Wpk, fpk, prob->K, 64, cs) != cudaSuccess)
-      return IGCONV_ERR_CUDA;
+      return cuda_error();
     if ((st = plan_fprop(p, bn, &vp, P, Q, bf16, Zp, Wpk, pw.strides)) != IGCONV_OK) return st;
     gW = Wpk;
   } else if (few) {
@@ -1713,12 +1723,12 @@ igconv_status_t conv2d_fprop_ws(const igconv_problem_t* prob, igconv_dtype_t dty
     if (prob->C < 8) {
       if (launch_pad_pixels8(X, ws, static_cast<long long>(prob->N) * prob->H * prob->W,
                              prob->C, cs) != cudaSuccess)
-        return IGCONV_ERR_CUDA;
+        return cuda_error();
       X8 = ws;
     }
     void* Wt8 = ws + fw.x_bytes;
     if (launch_filter_taps8(Wt, Wt8, prob->K, prob->R * prob->S, prob->C, bn, cs) != cudaSuccess)
-      return IGCONV_ERR_CUDA;
+      return cuda_error();
     if ((st = plan_fprop_taps(p, bn, prob, P, Q, bf16, X8, Wt8)) != IGCONV_OK) return st;
   } else if ((st = plan_fprop(p, bn, prob, P, Q, bf16, X, Wt)) != IGCONV_OK) {
     return st;
@@ -1764,7 +1774,7 @@ igconv_status_t conv2d_fprop_ws(const igconv_problem_t* prob, igconv_dtype_t dty
   p.out_bf16 = bf16;
   if (splits > 1) {
     set_conv_split(p, bn, splits, workspace);
-    if (launch_conv_gemm(p, bn, grid_for(p.units, dev), cs) != cudaSuccess) return IGCONV_ERR_CUDA;
+    if (launch_conv_gemm(p, bn, grid_for(p.units, dev), cs) != cudaSuccess) return cuda_error();
     return from_cuda(launch_conv_splitk_reduce(
         static_cast<const float*>(workspace), splits, p.ws_split_stride, p.ws_ld,
         static_cast<long long>(prob->N) * P * Q, prob->K, Y, bf16,
@@ -1877,7 +1887,7 @@ igconv_status_t conv2d_dgrad_ws(const igconv_problem_t* prob, igconv_dtype_t dty
     const int bf16 = dtype == IGCONV_BF16 ? 1 : 0;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (launch_few_pack_filter(Wt, Wz, fdp, prob->K, fdp.cz, cs) != cudaSuccess)
-      return IGCONV_ERR_CUDA;
+      return cuda_error();
     ConvGemmParams p;
     init_common(p, dev);
     int bn = 0;
@@ -1891,7 +1901,7 @@ igconv_status_t conv2d_dgrad_ws(const igconv_problem_t* prob, igconv_dtype_t dty
     p.pf_base = Wz;
     p.pf_bytes = static_cast<long long>(prob->K) * fdp.R2 * fdp.Sv * fdp.cz * 2;
     if (p.units > 0 && launch_conv_gemm(p, bn, grid_for(p.units, dev), cs) != cudaSuccess)
-      return IGCONV_ERR_CUDA;
+      return cuda_error();
     return from_cuda(launch_few_unpack_dx(dz, dX, fdp, prob->N, prob->H, prob->W, bf16,
                                           beta != 0.0f ? Cin : nullptr, beta, cs));
   }
@@ -1920,7 +1930,7 @@ igconv_status_t conv2d_dgrad_ws(const igconv_problem_t* prob, igconv_dtype_t dty
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (launch_pad_pixels8(Wt, W8, static_cast<long long>(prob->K) * prob->R * prob->S, prob->C,
                            cs) != cudaSuccess)
-      return IGCONV_ERR_CUDA;
+      return cuda_error();
     ConvGemmParams p;
     init_common(p, dev);
     int bn = 0;
@@ -1934,7 +1944,7 @@ igconv_status_t conv2d_dgrad_ws(const igconv_problem_t* prob, igconv_dtype_t dty
     p.pf_base = W8;
     p.pf_bytes = static_cast<long long>(prob->K) * prob->R * prob->S * 16;
     if (p.units > 0 && launch_conv_gemm(p, bn, grid_for(p.units, dev), cs) != cudaSuccess)
-      return IGCONV_ERR_CUDA;
+      return cuda_error();
     return from_cuda(launch_unpad_channels(dX8, dX,
                                            static_cast<long long>(prob->N) * prob->H * prob->W,
                                            prob->C, bf16, beta != 0.0f ? Cin : nullptr, beta, cs));
@@ -1966,7 +1976,7 @@ igconv_status_t conv2d_dgrad_ws(const igconv_problem_t* prob, igconv_dtype_t dty
     p.pf_base = Wt;
     p.pf_bytes = static_cast<long long>(prob->K) * prob->R * prob->S * prob->C * 2;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    if (launch_conv_gemm(p, bn, grid_for(p.units, dev), cs) != cudaSuccess) return IGCONV_ERR_CUDA;
+    if (launch_conv_gemm(p, bn, grid_for(p.units, dev), cs) != cudaSuccess) return cuda_error();
     return from_cuda(launch_conv_splitk_reduce(
         static_cast<const float*>(workspace), splits, p.ws_split_stride, p.ws_ld,
         static_cast<long long>(prob->N) * prob->H * prob->W, prob->C, dX, bf16,
@@ -2053,7 +2063,7 @@ igconv_status_t conv2d_wgrad(const igconv_problem_t* prob, igconv_dtype_t dtype,
     if (!workspace || workspace_bytes < pw.z_bytes + w.ws_bytes) return IGCONV_ERR_WORKSPACE;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     if (launch_few_pack_x(X, ws, fpk, prob->N, prob->H, prob->W, s) != cudaSuccess)
-      return IGCONV_ERR_CUDA;
+      return cuda_error();
     return run_wgrad(&vp, P, Q, w, bf16, ws, pw.strides, dY, ws + pw.z_bytes, dev,
                      prob->R * prob->S, prob->C, &fpk, dW, dw_dtype, Cin, alpha, beta, s);
   }
@@ -2119,7 +2129,7 @@ igconv_status_t conv2d_grouped_fprop(const igconv_problem_t* prob, int groups,
     return IGCONV_ERR_UNSUPPORTED;
   cudaError_t e = cudaSuccess;
   const int grid = dw_grid(p, dev, &e);
-  if (e != cudaSuccess) return IGCONV_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_error();
   return from_cuda(launch_depthwise(p, grid, static_cast<cudaStream_t>(stream)));
 }
 
@@ -2189,7 +2199,7 @@ igconv_status_t conv2d_grouped_fprop_ws(const igconv_problem_t* prob, int groups
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   if (launch_group_filter_dense(Wt, workspace, prob->K, prob->R * prob->S, prob->C,
                                 prob->C / groups, prob->K / groups, cs) != cudaSuccess)
-    return IGCONV_ERR_CUDA;
+    return cuda_error();
   constexpr int bn = 64;
   ConvGemmParams p;
   init_common(p, dev);
@@ -2259,7 +2269,7 @@ igconv_status_t conv2d_grouped_dgrad(const igconv_problem_t* prob, int groups,
     return IGCONV_ERR_UNSUPPORTED;
   cudaError_t e = cudaSuccess;
   const int grid = dw_grid(p, dev, &e);
-  if (e != cudaSuccess) return IGCONV_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_error();
   return from_cuda(launch_depthwise(p, grid, static_cast<cudaStream_t>(stream)));
 }
 
@@ -2304,7 +2314,7 @@ igconv_status_t conv2d_grouped_dgrad_ws(const igconv_problem_t* prob, int groups
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   if (launch_group_filter_dense(Wt, workspace, prob->K, prob->R * prob->S, prob->C,
                                 prob->C / groups, prob->K / groups, cs) != cudaSuccess)
-    return IGCONV_ERR_CUDA;
+    return cuda_error();
   ConvGemmParams p;
   init_common(p, dev);
   int bn = 64;
@@ -2380,12 +2390,12 @@ static igconv_status_t grouped_wgrad_gemm(const igconv_problem_t* prob, int grou
   const long long npq = static_cast<long long>(prob->N) * P * Q;
   if (!encode_2d(&p.mapB, dY, bf16, npq, prob->K)) return IGCONV_ERR_UNSUPPORTED;
   cudaError_t e = launch_conv_gemm(p, w.bn, grid_for(p.units, dev), s);
-  if (e != cudaSuccess) return IGCONV_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_error();
   float* dwexp = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + round256(w.ws_bytes));
   e = launch_wgrad_reduce(static_cast<const float*>(workspace), w.splits, p.ws_split_stride,
                           w.N_pad, w.rs * w.cpad, prob->K, 0, prob->K, w.rs, w.cpad, w.cpad,
                           dwexp, 2, nullptr, alpha, 0.0f, s);
-  if (e != cudaSuccess) return IGCONV_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_error();
   const int dwt = dw_dtype == IGCONV_F32 ? 2 : (dw_dtype == IGCONV_BF16 ? 1 : 0);
   return from_cuda(launch_group_extract(dwexp, dW, dwt, beta != 0.0f ? Cin : nullptr, beta,
                                         prob->K, w.rs, prob->C / groups, prob->K / groups,
@@ -2461,7 +2471,7 @@ igconv_status_t conv2d_grouped_wgrad(const igconv_problem_t* prob, int groups,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int grid = p.chunks * p.splits * (cg > 1 ? prob->R * prob->S : 1);
   cudaError_t e = launch_depthwise(p, grid, s);
-  if (e != cudaSuccess) return IGCONV_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_error();
   const int dwt = dw_dtype == IGCONV_F32 ? 2 : (dw_dtype == IGCONV_BF16 ? 1 : 0);
   e = launch_dw_wgrad_reduce(p.ws, p.splits, prob->R * prob->S, prob->C, cg, dW, dwt,
                              beta != 0.0f ? Cin : nullptr, alpha, beta, s);
@@ -2849,7 +2859,7 @@ igconv_status_t conv3d_wgrad(const igconv_problem3d_t* prob, igconv_dtype_t dtyp
   if (!encode_2d(&p.mapB, dY, bf16, npq, prob->K)) return IGCONV_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_conv_gemm(p, w.bn, grid_for(p.units, dev), s);
-  if (e != cudaSuccess) return IGCONV_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_error();
   const int dwt = dw_dtype == IGCONV_F32 ? 2 : (dw_dtype == IGCONV_BF16 ? 1 : 0);
   const int xext = w.rs * w.cpad;
   e = launch_wgrad_reduce(static_cast<const float*>(workspace), w.splits, p.ws_split_stride,
@@ -2972,9 +2982,9 @@ igconv_status_t conv2d_fprop_int8(const igconv_problem_t* prob, const int8_t* X,
   }
 
   cudaError_t e = launch_i8_to_f16(X, Xh, xcount, s);
-  if (e != cudaSuccess) return IGCONV_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_error();
   e = launch_i8_to_f16(Wt, Wh, wcount, s);
-  if (e != cudaSuccess) return IGCONV_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_error();
   e = launch_conv_gemm(p, bn, grid_for(p.units, dev), s);
   if (e != cudaSuccess || part == nullptr) return from_cuda(e);
   return from_cuda(launch_conv_splitk_reduce_i8(part, ip.splits, p.ws_split_stride, p.ws_ld,
@@ -3038,9 +3048,9 @@ igconv_status_t conv2d_dgrad_int8(const igconv_problem_t* prob, const int8_t* dY
   p.alpha = 1.0f;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_i8_to_f16(dY, dYh, ycount, s);
-  if (e != cudaSuccess) return IGCONV_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_error();
   e = launch_i8_to_f16(Wt, Wh, wcount, s);
-  if (e != cudaSuccess) return IGCONV_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_error();
   if (p.units == 0) return IGCONV_OK;
   return from_cuda(launch_conv_gemm(p, bn, grid_for(p.units, dev), s));
 }
@@ -3121,11 +3131,11 @@ igconv_status_t conv2d_wgrad_int8(const igconv_problem_t* prob, const int8_t* X,
   if (!encode_2d(&p.mapB, dYh, 0, npq, prob->K)) return IGCONV_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_i8_to_f16(X, Xh, xcount, s);
-  if (e != cudaSuccess) return IGCONV_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_error();
   e = launch_i8_to_f16(dY, dYh, ycount, s);
-  if (e != cudaSuccess) return IGCONV_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_error();
   e = launch_conv_gemm(p, w.bn, grid_for(p.units, dev), s);
-  if (e != cudaSuccess) return IGCONV_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_error();
   const int xext = w.rs * w.cpad;
   return from_cuda(launch_wgrad_reduce_i32(static_cast<const int*>(part), w.splits,
                                            p.ws_split_stride, w.N_pad,
@@ -3222,11 +3232,11 @@ igconv_status_t conv2d_fprop_winograd(const igconv_problem_t* prob, igconv_dtype
 
   cudaError_t e = launch_wino_input(X, V, prob->N, prob->H, prob->W, prob->C, w.TH, w.TW,
                                     prob->pad_h, prob->pad_w, bf16, s);
-  if (e != cudaSuccess) return IGCONV_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_error();
   e = launch_wino_filter(Wt, U, prob->K, prob->C, bf16, s);
-  if (e != cudaSuccess) return IGCONV_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_error();
   e = launch_conv_gemm(p, bn, grid_for(p.units, dev), s);
-  if (e != cudaSuccess) return IGCONV_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_error();
   return from_cuda(launch_wino_output(Mx, Y, beta != 0.0f ? Cin : nullptr, bias, prob->N, P, Q,
                                       prob->K, w.TH, w.TW, alpha, beta, relu ? 1 : 0, bf16, s));
 }
@@ -3270,13 +3280,13 @@ igconv_status_t igconv_get_device_status(void* stream) {
   if (st != IGCONV_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   unsigned int word = 0;
-  if (cudaStreamSynchronize(s) != cudaSuccess) return IGCONV_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return cuda_error();
   if (cudaMemcpy(&word, dev->status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
-    return IGCONV_ERR_CUDA;
+    return cuda_error();
   if (word != 0) {
     const unsigned int zero = 0;
     if (cudaMemcpy(dev->status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
-      return IGCONV_ERR_CUDA;
+      return cuda_error();
     return IGCONV_ERR_DEVICE_TIMEOUT;
   }
   return IGCONV_OK;
