@@ -7,8 +7,13 @@ with inputs already resident in HBM.  The metric is the one the workloads are
 quoted on: convolution TFLOP/s (2*N*P*Q*K*C*R*S per pass), and the fraction of
 the dense bf16 tensor peak.
 
-Prints one JSON line (rank 0).  Keys beyond the required ones:
-  passes      per-pass TFLOP/s over the step
+Prints one JSON line (rank 0).  The step is timed as a CUDA graph of its
+calls between two events, with nothing between the kernels.  Keys beyond
+the required ones:
+  passes      per-pass TFLOP/s, from graphs of the five calls of one pass
+              kind each
+  layers      per-call times, from a graph with an event pair around every
+              call (those event nodes add a few us per call)
   roofline    the implicit-GEMM kernel (fprop + dgrad launches, which are
               single-kernel calls) against the measured bf16 peak
   cpu_baseline the CPU oracle, timed on a bounded sample of the same workload
