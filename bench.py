@@ -556,6 +556,17 @@ def check_outputs(layers, samples, seed):
             "bound": "|err_i| <= ulp(out_i) + 2^-10 * sum|x*w|_i against the fp64 oracle"}
 
 
+def job_rate(step_flops, steps, total_ms, world, device):
+    """Whole-job TFLOP/s over all ranks and the time it is taken over: the
+    slowest rank's time (max over ranks) and the work of every rank (each
+    rank runs the same step on its own GPU: weak scaling)."""
+    t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    total_ms = float(t.item())
+    return step_flops * steps * world / (total_ms * 1e-3) / 1e12, total_ms
+
+
 def run_ours(args, rank, world, local_rank):
     import convolution_implicit_gemm_gb300 as igc
     device = torch.device("cuda", local_rank)
@@ -713,13 +724,8 @@ def run_ours(args, rank, world, local_rank):
         rows = measure_rows(args, device, stream)
         status["rows"] = require_device_ok(igc, "the rows")
 
-    # reduce across ranks: max time, summed work
-    t = torch.tensor([total_ms], dtype=torch.float64, device=device)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    total_ms = float(t.item())
+    value, total_ms = job_rate(step_flops, args.steps, total_ms, world, device)
     ms_per_step = total_ms / args.steps
-    value = step_flops * args.steps * world / (total_ms * 1e-3) / 1e12
     layer_rows = {n: {k: {"us": v * 1e3,
                           "TFLOP/s": next(L.flops for L in layers if L.name == n) / (v * 1e-3) / 1e12}
                       for k, v in d.items()} for n, d in per_layer.items()}
